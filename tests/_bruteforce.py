@@ -1,0 +1,93 @@
+"""Pure-Python brute-force evaluation of the SSB objective for tiny inputs.
+
+Written independently of the vectorised oracle: direct double sums for both
+transforms on the full grid (no half-plane, no mirror rule, no FFT), per-point
+transfer evaluation with cmath, and explicit moment loops.  Only usable for N <= 8
+and a handful of BF pixels.
+"""
+import cmath
+import math
+
+
+def _signed(q, n):
+    # fftfreq ordering: 0..n/2-1 positive, n/2..n-1 negative (Nyquist negative)
+    return q if q < n // 2 else q - n
+
+
+def _probe(ax, ay, lam, semi, da, c10, c12, phi12):
+    amp = min(1.0, max(0.0, (semi - math.hypot(ax, ay)) / da + 0.5))
+    ph = (math.pi / lam) * (c10 * (ax * ax + ay * ay)
+                            + c12 * ((ax * ax - ay * ay) * math.cos(2 * phi12)
+                                     + 2 * ax * ay * math.sin(2 * phi12)))
+    return amp, ph
+
+
+def objective_loops(counts, geom, theta, mode="ssb2"):
+    n = int(geom.scan_n)
+    p = n * n
+    lam = geom.wavelength_A
+    semi = geom.semiangle_mrad * 1e-3
+    da = geom.det_sampling_mrad * 1e-3
+    c10, c12, phi12, rot = theta[0] * 10.0, theta[1] * 10.0, theta[2], theta[3]
+    cr, sr = math.cos(rot), math.sin(rot)
+    nb = len(geom.bf_det_yx)
+    s1 = [[0.0] * n for _ in range(n)]
+    s2 = [[0.0] * n for _ in range(n)]
+    phases = []
+    for k in range(nb):
+        ay_k = float(geom.bf_det_yx[k][0]) * da
+        ax_k = float(geom.bf_det_yx[k][1]) * da
+        img = [[float(counts[k][y][x]) for x in range(n)] for y in range(n)]
+        # forward DFT on the full grid
+        spec = [[0j] * n for _ in range(n)]
+        for qy in range(n):
+            for qx in range(n):
+                acc = 0j
+                for y in range(n):
+                    for x in range(n):
+                        acc += img[y][x] * cmath.exp(-2j * math.pi * (qy * y + qx * x) / n)
+                spec[qy][qx] = acc
+        # correction at each signed frequency
+        ak_amp, ak_ph = _probe(ax_k, ay_k, lam, semi, da, c10, c12, phi12)
+        corr = [[0j] * n for _ in range(n)]
+        for qy in range(n):
+            for qx in range(n):
+                if qx == 0 and qy == 0:
+                    corr[qy][qx] = spec[0][0]
+                    continue
+                fx = _signed(qx, n) / (n * geom.scan_step_A)
+                fy = _signed(qy, n) / (n * geom.scan_step_A)
+                lx = lam * (cr * fx - sr * fy)
+                ly = lam * (sr * fx + cr * fy)
+                am, pm = _probe(ax_k - lx, ay_k - ly, lam, semi, da, c10, c12, phi12)
+                ap, pp = _probe(ax_k + lx, ay_k + ly, lam, semi, da, c10, c12, phi12)
+                if mode == "ssb2":
+                    term1 = ak_amp * am * cmath.exp(1j * (pm - ak_ph))
+                    term2 = ak_amp * ap * cmath.exp(1j * (ak_ph - pp))
+                    gam = term1 - term2
+                    corr[qy][qx] = 0j if abs(gam) == 0.0 else spec[qy][qx] * gam.conjugate() / abs(gam)
+                elif mode == "ssb1":
+                    corr[qy][qx] = (spec[qy][qx] * cmath.exp(1j * (ak_ph - pm))
+                                    if ak_amp * am > 0.0 else 0j)
+                else:
+                    corr[qy][qx] = spec[qy][qx]
+        # inverse DFT and phase
+        ph = [[0.0] * n for _ in range(n)]
+        for y in range(n):
+            for x in range(n):
+                acc = 0j
+                for qy in range(n):
+                    for qx in range(n):
+                        acc += corr[qy][qx] * cmath.exp(2j * math.pi * (qy * y + qx * x) / n)
+                acc /= p
+                v = math.atan2(acc.imag, acc.real)
+                ph[y][x] = v
+                s1[y][x] += v
+                s2[y][x] += v * v
+        phases.append(ph)
+    loss = 0.0
+    for y in range(n):
+        for x in range(n):
+            m = s1[y][x] / nb
+            loss += s2[y][x] / nb - m * m
+    return loss / p, phases

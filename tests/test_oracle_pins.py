@@ -1,0 +1,304 @@
+"""Pins of the float64 oracle against things other than itself: brute-force DFTs,
+Parseval, closed-form symmetries of the transfer, special cases that reduce to a
+known answer, a pure-Python brute force, the library variance, physics (recovery of
+the aberrations the generator used) and the numbers the pages print."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import ssb_synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_facts.json")
+
+
+def _geom(scan_n=32, det_n=24, radius=6.0, semiangle=20.0, subset=None):
+    w = ssb_synth.Workload("t", scan_n, det_n, radius, "u16", 200.0, 0.1,
+                           (50.0, 0.0, 0.0, 0.0), seed=7, trial_seed=8, n_trials=1,
+                           semiangle_mrad=semiangle)
+    return w, ssb_synth.make_geometry(w, bf_subset=subset)
+
+
+# ---------------------------------------------------------------- transforms
+
+@pytest.mark.parametrize("n", [4, 8, 16])
+def test_fft_matches_direct_dft(n):
+    rng = np.random.default_rng(n)
+    x = rng.standard_normal((n, n)) + 1j * rng.standard_normal((n, n))
+    ref_f = oracle.fft2_forward(x, direct=True)
+    ref_i = oracle.ifft2_inverse(x, direct=True)
+    assert np.allclose(oracle.fft2_forward(x), ref_f, rtol=0, atol=1e-12 * np.abs(ref_f).max())
+    assert np.allclose(oracle.ifft2_inverse(x), ref_i, rtol=0, atol=1e-12 * np.abs(ref_i).max())
+    # direct DFT from its definition, one entry by explicit summation
+    j = np.arange(n)
+    e = np.sum(x * np.exp(-2j * np.pi * (3 % n * j[:, None] + 1 * j[None, :]) / n))
+    assert abs(ref_f[3 % n, 1] - e) < 1e-10 * abs(e) + 1e-12
+
+
+@pytest.mark.parametrize("n", [4, 8, 16, 32])
+def test_parseval_and_half_plane_mirror(n):
+    rng = np.random.default_rng(10 + n)
+    img = rng.integers(0, 1000, size=(n, n))
+    gh = oracle.g_plane(img)
+    full = oracle.full_plane(gh)
+    ref = np.fft.fft2(img.astype(np.float64))
+    assert np.abs(full - ref).max() <= 1e-12 * np.abs(ref).max()
+    # Parseval: sum |x|^2 = sum |X|^2 / P
+    assert math.isclose(float(np.sum(img.astype(float) ** 2)),
+                        float(np.sum(np.abs(full) ** 2)) / (n * n), rel_tol=1e-12)
+    if n <= 16:
+        ghd = oracle.g_plane(img, direct=True)
+        assert np.abs(ghd - gh).max() <= 1e-10 * np.abs(gh).max()
+
+
+# ---------------------------------------------------------------- transfer
+
+def test_transfer_anti_hermitian_off_nyquist():
+    """Gamma(-Q) = -conj(Gamma(Q)) for any theta wherever -Q is on the grid with the
+    negated signed frequency, i.e. off the Nyquist row and column."""
+    _, geom = _geom()
+    # a coarser scan puts the Nyquist lines inside the transfer band (|lambda Q| < 2 alpha_c)
+    geom.scan_step_A *= 1.5
+    g = oracle.Geom.from_obj(geom)
+    theta = (37.0, 12.0, 0.4, 0.3)
+    n = g.n
+    worst_nyquist = 0.0
+    for k in range(0, g.n_bf, 7):
+        gam = oracle.transfer(g, k, theta)
+        idx = (-np.arange(n)) % n
+        mirrored = gam[idx][:, idx]
+        keep = np.ones((n, n), bool)
+        keep[n // 2, :] = False
+        keep[:, n // 2] = False
+        assert np.abs(gam + np.conj(mirrored))[keep].max() < 1e-12
+        worst_nyquist = max(worst_nyquist, np.abs(gam + np.conj(mirrored))[~keep].max())
+    # on the Nyquist lines the relation fails: those bins have no partner
+    assert worst_nyquist > 1e-3
+
+
+def test_transfer_real_at_zero_aberration():
+    _, geom = _geom()
+    g = oracle.Geom.from_obj(geom)
+    gam = oracle.transfer(g, 10, (0.0, 0.0, 0.0, 0.25))
+    assert np.abs(gam.imag).max() == 0.0
+
+
+def test_zero_transfer_gives_exact_zero(tiny_data):
+    _, geom, counts, _ = tiny_data
+    g = oracle.Geom.from_obj(geom)
+    theta = (20.0, 5.0, 0.1, 0.0)
+    k = 3
+    gam = oracle.transfer(g, k, theta)
+    c = oracle.corrected_spectrum(g, k, oracle.full_plane(oracle.g_plane(counts[k])), theta)
+    zero = np.abs(gam) == 0.0
+    zero[0, 0] = False
+    assert zero.sum() > 0
+    assert np.all(c[zero] == 0)
+    assert c[0, 0] == oracle.g_plane(counts[k])[0, 0]
+
+
+def test_identity_correction_returns_the_bf_image(tiny_data):
+    """With the correction disabled C = G is Hermitian, so the inverse transform is the
+    real, non-negative BF image itself and every phase (and the loss) vanishes."""
+    _, geom, counts, _ = tiny_data
+    res = oracle.objective(geom, (0, 0, 0, 0), counts=counts[:12], mode="identity",
+                           want_phases=True, bf_range=(0, 12))
+    assert res["loss"] < 1e-24
+    assert np.abs(res["phases"]).max() < 1e-12
+    g = oracle.Geom.from_obj(geom)
+    _, c = oracle.bf_phase(oracle.corrected_spectrum(g, 2, oracle.full_plane(oracle.g_plane(counts[2])),
+                                                     (0, 0, 0, 0), "identity"))
+    assert np.abs(c.real - counts[2]).max() < 1e-9 * counts[2].max()
+    assert np.abs(c.imag).max() < 1e-12 * counts[2].max()
+
+
+def test_ssb2_real_part_is_dc_without_nyquist_lines(tiny_data):
+    """Off DC and the Nyquist lines C is anti-Hermitian, so Re c_k = G_k(0)/P."""
+    _, geom, counts, _ = tiny_data
+    g = oracle.Geom.from_obj(geom)
+    n = g.n
+    theta = (60.0, 8.0, 0.7, 0.2)
+    for k in (0, 40, 112):
+        gh = oracle.g_plane(counts[k])
+        c = oracle.corrected_spectrum(g, k, oracle.full_plane(gh), theta)
+        c[n // 2, :] = 0
+        c[:, n // 2] = 0
+        r = np.fft.ifft2(c)
+        assert np.abs(r.real - gh[0, 0].real / (n * n)).max() < 1e-12 * gh[0, 0].real / (n * n)
+        assert np.abs(r.imag).max() > 1e-6 * gh[0, 0].real / (n * n)
+
+
+def test_inactive_bf_has_exactly_zero_phase():
+    """A BF pixel outside the probe aperture keeps only the positive DC term."""
+    w, geom = _geom()
+    geom.semiangle_mrad = 12.0  # probe aperture smaller than the BF disk
+    _, counts, _ = ssb_synth.simulate_counts_numpy(w, geom=geom)
+    g = oracle.Geom.from_obj(geom)
+    amp = oracle.aperture(g.alpha_x, g.alpha_y, g.semi, g.dalpha)
+    inactive = np.nonzero(amp == 0)[0]
+    assert len(inactive) > 0
+    res = oracle.objective(geom, (30.0, 5.0, 0.2, 0.1), counts=counts, want_phases=True)
+    assert np.all(res["phases"][inactive] == 0.0)
+    assert res["n_bf"] == g.n_bf  # still in the normalisation
+
+
+def test_ssb1_equals_ssb2_where_only_one_sideband_overlaps(tiny_data):
+    _, geom, counts, _ = tiny_data
+    g = oracle.Geom.from_obj(geom)
+    theta = (45.0, 6.0, 0.3, 0.15)
+    k = 30
+    gf = oracle.full_plane(oracle.g_plane(counts[k]))
+    c1 = oracle.corrected_spectrum(g, k, gf, theta, "ssb1")
+    c2 = oracle.corrected_spectrum(g, k, gf, theta, "ssb2")
+    lqx, lqy = oracle.rotated_frequencies(g, theta[3])
+    ap = oracle.aperture(g.alpha_x[k] + g.lam * lqx, g.alpha_y[k] + g.lam * lqy, g.semi, g.dalpha)
+    am = oracle.aperture(g.alpha_x[k] - g.lam * lqx, g.alpha_y[k] - g.lam * lqy, g.semi, g.dalpha)
+    single = (ap == 0) & (am > 0)
+    assert single.sum() > 10
+    assert np.abs(c1 - c2)[single].max() < 1e-9 * np.abs(gf).max()
+
+
+def test_conjugate_branch():
+    """(C10, C12, phi12, rot) -> (-C10, -C12, phi12, rot + pi) maps Gamma -> -Gamma, so
+    c -> 2 DC/P - c and phi -> -phi up to the Nyquist-line terms."""
+    w = ssb_synth.WORKLOADS["tiny"]
+    geom, counts, _ = ssb_synth.simulate_counts_numpy(w)
+    theta = (70.0, 9.0, 0.5, 0.2)
+    conj = (-70.0, -9.0, 0.5, 0.2 + math.pi)
+    a = oracle.objective(geom, theta, counts=counts)["loss"]
+    b = oracle.objective(geom, conj, counts=counts)["loss"]
+    page = json.load(open(GOLDEN))["conjugate_branch_rel"]["value"]
+    assert a > 0
+    assert abs(a - b) / a < 1e3 * page  # Nyquist terms only
+    # with the Nyquist lines removed the two branches agree to rounding
+    gm = oracle.Geom.from_obj(geom)
+    n = gm.n
+    for k in (0, 50, 100):
+        gf = oracle.full_plane(oracle.g_plane(counts[k]))
+        ca = oracle.corrected_spectrum(gm, k, gf, theta)
+        cb = oracle.corrected_spectrum(gm, k, gf, conj)
+        for cc in (ca, cb):
+            cc[n // 2, :] = 0
+            cc[:, n // 2] = 0
+        pa = np.angle(np.fft.ifft2(ca))
+        pb = np.angle(np.fft.ifft2(cb))
+        assert np.abs(pa + pb).max() < 1e-10
+
+
+# ---------------------------------------------------------------- objective
+
+def test_loss_is_mean_population_variance(tiny_data):
+    _, geom, counts, _ = tiny_data
+    res = oracle.objective(geom, (40.0, 3.0, 0.2, 0.0), counts=counts, want_phases=True)
+    ref = float(np.mean(np.var(res["phases"], axis=0)))
+    assert math.isclose(res["loss"], ref, rel_tol=1e-12)
+    assert np.allclose(res["mean_phase"], np.mean(res["phases"], axis=0), atol=1e-14)
+
+
+def test_object_linearity(tiny_data):
+    _, geom, counts, _ = tiny_data
+    theta = (50.0, 0.0, 0.0, 0.0)
+    res = oracle.objective(geom, theta, counts=counts, want_object=True)
+    obj2 = oracle.object_from_spectrum_sum(geom, theta, counts)
+    assert np.abs(res["object"] - obj2).max() < 1e-12 * np.abs(obj2).max()
+
+
+@pytest.mark.parametrize("mode", ["ssb2", "ssb1"])
+def test_oracle_matches_pure_python_brute_force(mode):
+    import _bruteforce
+    w, geom = _geom(scan_n=8, det_n=8, radius=2.0)
+    geom = ssb_synth.make_geometry(w, bf_subset=np.array([0, 3, 6, 9, 12]))
+    _, counts, _ = ssb_synth.simulate_counts_numpy(w, geom=geom)
+    theta = (80.0, 14.0, 0.9, 0.35)
+    loss_bf, phases_bf = _bruteforce.objective_loops(counts, geom, theta, mode=mode)
+    res = oracle.objective(geom, theta, counts=counts, mode=mode, want_phases=True)
+    assert np.abs(res["phases"] - np.array(phases_bf)).max() < 1e-9
+    assert math.isclose(res["loss"], loss_bf, rel_tol=1e-10)
+    resd = oracle.objective(geom, theta, counts=counts, mode=mode, direct=True)
+    assert math.isclose(resd["loss"], loss_bf, rel_tol=1e-10)
+
+
+# ---------------------------------------------------------------- physics
+
+def _scan_argmin(geom, counts, base, index, values):
+    losses = []
+    for v in values:
+        th = list(base)
+        th[index] = v
+        losses.append(oracle.objective(geom, th, counts=counts)["loss"])
+    return values[int(np.argmin(losses))], losses
+
+
+def test_defocus_recovery_tiny(tiny_data):
+    w, geom, counts, _ = tiny_data
+    values = np.arange(-200.0, 200.0 + 1e-9, 5.0)
+    best, losses = _scan_argmin(geom, counts, w.truth, 0, values)
+    assert abs(best - w.truth[0]) <= 5.0
+    # the conjugate defocus is not a minimum of the loss at fixed rotation
+    assert losses[int(np.argmin(np.abs(values + w.truth[0])))] > min(losses) * 1.05
+
+
+@pytest.mark.slow
+def test_rotation_and_astigmatism_recovery():
+    w = ssb_synth.Workload("rot", 48, 32, 8.0, "u16", 400.0, 0.2,
+                           (-60.0, 20.0, math.radians(40.0), math.radians(25.0)),
+                           seed=11, trial_seed=12, n_trials=1)
+    geom, counts, _ = ssb_synth.simulate_counts_numpy(w)
+    rot_values = np.radians(np.arange(0.0, 50.1, 2.5))
+    best_rot, _ = _scan_argmin(geom, counts, w.truth, 3, rot_values)
+    assert abs(best_rot - w.truth[3]) <= math.radians(2.5) + 1e-9
+    c12_values = np.arange(0.0, 40.1, 2.5)
+    best_c12, _ = _scan_argmin(geom, counts, w.truth, 1, c12_values)
+    assert abs(best_c12 - w.truth[1]) <= 2.5
+    phi_values = np.radians(np.arange(0.0, 180.0, 7.5))
+    best_phi, _ = _scan_argmin(geom, counts, w.truth, 2, phi_values)
+    d = abs(best_phi - w.truth[2]) % math.pi
+    assert min(d, math.pi - d) <= math.radians(7.5) + 1e-9
+    c10_values = np.arange(-100.0, 0.1, 5.0)
+    best_c10, _ = _scan_argmin(geom, counts, w.truth, 0, c10_values)
+    assert abs(best_c10 - w.truth[0]) <= 5.0
+
+
+def test_mean_phase_tracks_the_object(tiny_data):
+    w, geom, counts, phi = tiny_data
+    res = oracle.objective(geom, w.truth, counts=counts)
+    mp = res["mean_phase"]
+    # compare within the transfer band (|lambda Q| < 2 alpha_c)
+    g = oracle.Geom.from_obj(geom)
+    qx, qy = oracle.scan_frequencies(g)
+    band = (g.lam * np.sqrt(qx ** 2 + qy ** 2) < 2 * g.semi)
+    band[0, 0] = False
+    lp = np.fft.ifft2(np.fft.fft2(phi) * band).real
+    cc = np.corrcoef(mp.ravel(), lp.ravel())[0, 1]
+    assert cc > 0.9
+
+
+# ---------------------------------------------------------------- page facts
+
+def test_full_workload_geometry_matches_the_pages():
+    facts = json.load(open(GOLDEN))
+    w = ssb_synth.WORKLOADS["full"]
+    geom = ssb_synth.make_geometry(w)
+    assert w.scan_n == facts["scan_n"]["value"]
+    assert w.det_n == facts["det_n"]["value"]
+    assert geom.n_bf == facts["full_bf_pixels"]["value"]
+    assert geom.n_bf * w.scan_n ** 2 == facts["samples_per_objective"]["value"]
+    assert w.scan_n // 2 + 1 == facts["half_plane_columns"]["value"]
+    assert (w.scan_n // 2 + 1) + w.scan_n == facts["ifft_count_per_bf"]["value"]
+
+
+@pytest.mark.parametrize("name,expected", [("tiny", 113), ("small", 709), ("medium", 2289)])
+def test_workload_bf_counts(name, expected):
+    assert ssb_synth.make_geometry(ssb_synth.WORKLOADS[name]).n_bf == expected
+
+
+def test_generator_dose_and_determinism():
+    w = ssb_synth.WORKLOADS["tiny"]
+    g1, c1, _ = ssb_synth.simulate_counts_numpy(w)
+    g2, c2, _ = ssb_synth.simulate_counts_numpy(w)
+    assert np.array_equal(c1, c2)
+    assert c1.dtype == np.uint16
+    assert abs(c1.mean() / w.mean_count - 1) < 0.01
