@@ -210,24 +210,26 @@ def bf_phase(c_spec: np.ndarray, direct=False):
 def _partial(args):
     """Moments and object sum over a contiguous range of BF pixels, ascending k."""
     (geom_args, k0, k1, data, data_is_g, theta, mode, direct, want_object,
-     want_phases) = args
+     want_phases, branch_tol) = args
     g = Geom(*geom_args)
     n = g.n
     s1 = np.zeros((n, n))
     s2 = np.zeros((n, n))
     osum = np.zeros((n, n), dtype=np.complex128) if want_object else None
     phases = [] if want_phases else None
+    near_pi = np.zeros((n, n), dtype=bool)
     for i, k in enumerate(range(k0, k1)):
         gh = data[i] if data_is_g else g_plane(data[i], direct=direct)
         cs = corrected_spectrum(g, k, full_plane(gh), theta, mode)
         phi, c = bf_phase(cs, direct=direct)
         s1 += phi
         s2 += phi * phi
+        near_pi |= np.abs(np.abs(phi) - np.pi) < branch_tol
         if want_object:
             osum += c
         if want_phases:
             phases.append(phi)
-    return s1, s2, osum, phases
+    return s1, s2, osum, phases, near_pi
 
 
 def _geom_args(g: Geom):
@@ -237,7 +239,7 @@ def _geom_args(g: Geom):
 
 def objective(geom, theta, counts=None, g_half=None, mode="ssb2", direct=False,
               want_object=False, want_phases=False, workers: int = 1,
-              bf_range: Optional[Sequence[int]] = None):
+              bf_range: Optional[Sequence[int]] = None, branch_tol: float = 1e-4):
     """Evaluate the SSB phase-variance objective in float64.
 
     geom:   ssb_synth.Geometry-like object or Geom
@@ -246,7 +248,11 @@ def objective(geom, theta, counts=None, g_half=None, mode="ssb2", direct=False,
              processes; chunk partials are added in ascending chunk order.
     bf_range: optional (k0, k1) restricting the sum (the normalisation then uses
              the restricted count).
-    Returns a dict with loss, mean_phase, s1, s2, n_bf and optionally object / phases.
+    branch_tol: pixels where some BF phase lies within this distance of +-pi are
+             flagged in "branch_cut" (a float32 evaluation may land on the other side
+             of the atan2 branch cut there).
+    Returns a dict with loss, mean_phase, s1, s2, n_bf, branch_cut and optionally
+    object / phases.
     """
     g = geom if isinstance(geom, Geom) else Geom.from_obj(geom)
     theta = tuple(float(x) for x in theta)
@@ -256,12 +262,13 @@ def objective(geom, theta, counts=None, g_half=None, mode="ssb2", direct=False,
     ga = _geom_args(g)
     if workers <= 1 or k1 - k0 < 2 * workers:
         parts = [_partial((ga, k0, k1, data[k0:k1], data_is_g, theta, mode, direct,
-                           want_object, want_phases))]
+                           want_object, want_phases, branch_tol))]
     else:
         import multiprocessing as mp
         bounds = np.linspace(k0, k1, workers + 1).astype(int)
         jobs = [(ga, int(a), int(b), data[a:b], data_is_g, theta, mode, direct,
-                 want_object, want_phases) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+                 want_object, want_phases, branch_tol)
+                for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
         with mp.get_context("spawn").Pool(len(jobs)) as pool:
             parts = pool.map(_partial, jobs)
     n = g.n
@@ -269,7 +276,9 @@ def objective(geom, theta, counts=None, g_half=None, mode="ssb2", direct=False,
     s2 = np.zeros((n, n))
     osum = np.zeros((n, n), dtype=np.complex128) if want_object else None
     phases = [] if want_phases else None
+    near_pi = np.zeros((n, n), dtype=bool)
     for p in parts:
+        near_pi |= p[4]
         s1 += p[0]
         s2 += p[1]
         if want_object:
@@ -278,7 +287,8 @@ def objective(geom, theta, counts=None, g_half=None, mode="ssb2", direct=False,
             phases.extend(p[3])
     nb = k1 - k0
     loss = float(np.mean(s2 / nb - (s1 / nb) ** 2))
-    out = {"loss": loss, "mean_phase": s1 / nb, "s1": s1, "s2": s2, "n_bf": nb}
+    out = {"loss": loss, "mean_phase": s1 / nb, "s1": s1, "s2": s2, "n_bf": nb,
+           "branch_cut": near_pi}
     if want_object:
         out["object"] = osum / nb
         out["object_phase"] = np.angle(osum / nb)

@@ -1,0 +1,390 @@
+// C ABI of the SSB library: argument validation, context ownership, orchestration.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "ssb_device.cuh"
+#include "ssb_internal.h"
+
+namespace ssb {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+static thread_local std::string g_last_error;
+
+static ssb_status fail(ssb_status st, const std::string &msg) {
+    g_last_error = msg;
+    return st;
+}
+
+static ssb_status cuda_fail(cudaError_t e, const char *what) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    (void)cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? SSB_ERR_OOM : SSB_ERR_CUDA;
+}
+
+#define SSB_CK(call)                                         \
+    do {                                                     \
+        cudaError_t _e = (call);                             \
+        if (_e != cudaSuccess) return cuda_fail(_e, #call);  \
+    } while (0)
+
+// Makes the context's device current for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace ssb
+
+using namespace ssb;
+
+struct ssb_ctx {
+    int dev = 0;
+    int N = 0, n_bf = 0, B = 0;
+    double step = 0, lam = 0, semi = 0, dalpha = 0;
+    ssb_transfer transfer = SSB_TRANSFER_SSB2;
+    float2 *G = nullptr;
+    float4 *kgeo = nullptr;
+    double2 *kalpha = nullptr;
+    uint2 *kturn = nullptr;
+    float2 *E = nullptr;
+    float2 *tw = nullptr;
+    float2 *X = nullptr;
+    double *S1 = nullptr, *S2 = nullptr;
+    double2 *Osum = nullptr;
+    double *loss = nullptr;
+    int loss_cap = 0;
+    int *flag = nullptr;
+    size_t g_bytes = 0, scratch_bytes = 0;
+
+    ObjectiveArgs args() const {
+        ObjectiveArgs a;
+        a.N = N;
+        a.n_bf = n_bf;
+        a.G = G;
+        a.kgeo = kgeo;
+        a.kalpha = kalpha;
+        a.kturn = kturn;
+        a.E = E;
+        a.tw = tw;
+        a.X = X;
+        a.B = B;
+        a.S1 = S1;
+        a.S2 = S2;
+        a.Osum = Osum;
+        a.loss = loss;
+        a.mode = transfer == SSB_TRANSFER_SSB1 ? 1 : 0;
+        a.step = step;
+        a.lam = lam;
+        a.semi = semi;
+        a.dalpha = dalpha;
+        return a;
+    }
+};
+
+static void free_ctx(ssb_ctx *c) {
+    if (!c) return;
+    void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->X,
+                    c->S1, c->S2, c->Osum, c->loss, c->flag};
+    for (void *p : ptrs)
+        if (p) cudaFree(p);
+    delete c;
+}
+
+static bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
+
+static bool valid_theta(const ssb_params &t) {
+    return std::isfinite(t.C10_nm) && std::isfinite(t.C12_nm) && std::isfinite(t.phi12_rad) &&
+           std::isfinite(t.rotation_rad);
+}
+
+template <typename T>
+static cudaError_t dev_alloc(T **p, size_t count, size_t *acc) {
+    *acc += count * sizeof(T);
+    return cudaMalloc((void **)p, count * sizeof(T));
+}
+
+static ssb_status check_flag(ssb_ctx *c, cudaStream_t s) {
+    int h = 0;
+    SSB_CK(cudaMemcpyAsync(&h, c->flag, sizeof(int), cudaMemcpyDeviceToHost, s));
+    SSB_CK(cudaStreamSynchronize(s));
+    if (h & 1) {
+        SSB_CK(cudaMemsetAsync(c->flag, 0, sizeof(int), s));
+        return fail(SSB_ERR_ARG, "a count exceeds 2^24 and cannot be converted to float32 exactly");
+    }
+    if (h) {
+        SSB_CK(cudaMemsetAsync(c->flag, 0, sizeof(int), s));
+        return fail(SSB_ERR_DEVICE_FLAG, "kernel error flag " + std::to_string(h));
+    }
+    return SSB_OK;
+}
+
+extern "C" {
+
+const char *ssb_status_string(ssb_status s) {
+    switch (s) {
+        case SSB_OK: return "SSB_OK";
+        case SSB_ERR_ARG: return "SSB_ERR_ARG";
+        case SSB_ERR_UNSUPPORTED: return "SSB_ERR_UNSUPPORTED";
+        case SSB_ERR_OOM: return "SSB_ERR_OOM";
+        case SSB_ERR_CUDA: return "SSB_ERR_CUDA";
+        case SSB_ERR_TIMEOUT: return "SSB_ERR_TIMEOUT";
+        case SSB_ERR_DEVICE_FLAG: return "SSB_ERR_DEVICE_FLAG";
+    }
+    return "SSB_ERR_UNKNOWN";
+}
+
+const char *ssb_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t ssb_kernel_launches(void) { return g_launches.load(); }
+
+ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtype,
+                       int counts_on_device, ssb_transfer transfer, void *cuda_stream,
+                       ssb_ctx **out) {
+    g_last_error.clear();
+    if (!out) return fail(SSB_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    if (!g || !counts) return fail(SSB_ERR_ARG, "geometry or counts is NULL");
+    const int N = g->scan_n;
+    if (N != 32 && N != 64 && N != 128 && N != 256 && N != 512)
+        return fail(SSB_ERR_UNSUPPORTED, "scan_n must be 32, 64, 128, 256 or 512");
+    if (g->n_bf < 1) return fail(SSB_ERR_ARG, "n_bf must be >= 1");
+    if (!g->bf_det_yx) return fail(SSB_ERR_ARG, "bf_det_yx is NULL");
+    if (!finite_pos(g->scan_step_A) || !finite_pos(g->wavelength_A) ||
+        !finite_pos(g->semiangle_mrad) || !finite_pos(g->det_sampling_mrad))
+        return fail(SSB_ERR_ARG, "geometry scalars must be finite and positive");
+    if (dtype != SSB_U16 && dtype != SSB_U32) return fail(SSB_ERR_ARG, "unknown dtype");
+    if (transfer != SSB_TRANSFER_SSB2 && transfer != SSB_TRANSFER_SSB1)
+        return fail(SSB_ERR_ARG, "unknown transfer");
+    for (int k = 0; k < 2 * g->n_bf; ++k)
+        if (!std::isfinite(g->bf_det_yx[k])) return fail(SSB_ERR_ARG, "bf_det_yx has a non-finite entry");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+
+    ssb_ctx *c = new (std::nothrow) ssb_ctx();
+    if (!c) return fail(SSB_ERR_OOM, "host allocation failed");
+    SSB_CK(cudaGetDevice(&c->dev));
+    c->N = N;
+    c->n_bf = g->n_bf;
+    c->step = g->scan_step_A;
+    c->lam = g->wavelength_A;
+    c->semi = g->semiangle_mrad * 1e-3;
+    c->dalpha = g->det_sampling_mrad * 1e-3;
+    c->transfer = transfer;
+    const int H = N / 2 + 1;
+    const size_t P = (size_t)N * N;
+    const size_t per_bf_x = P * sizeof(float2);
+    c->B = (int)std::max<size_t>(1, std::min<size_t>((size_t)c->n_bf, (64u << 20) / per_bf_x));
+
+    ssb_status st = SSB_OK;
+    auto bail = [&](ssb_status code) {
+        free_ctx(c);
+        return code;
+    };
+    cudaError_t e;
+    size_t gb = 0, sb = 0;
+#define SSB_ALLOC(ptr, count, acc)                                       \
+    if ((e = dev_alloc(&(ptr), (count), &(acc))) != cudaSuccess) {       \
+        st = cuda_fail(e, "cudaMalloc " #ptr);                           \
+        return bail(st);                                                 \
+    }
+    SSB_ALLOC(c->G, (size_t)c->n_bf * H * N, gb);
+    SSB_ALLOC(c->kgeo, (size_t)c->n_bf, sb);
+    SSB_ALLOC(c->kalpha, (size_t)c->n_bf, sb);
+    SSB_ALLOC(c->kturn, (size_t)c->n_bf, sb);
+    SSB_ALLOC(c->E, P, sb);
+    SSB_ALLOC(c->tw, (size_t)N, sb);
+    SSB_ALLOC(c->X, (size_t)c->B * P, sb);
+    SSB_ALLOC(c->S1, P, sb);
+    SSB_ALLOC(c->S2, P, sb);
+    SSB_ALLOC(c->Osum, P, sb);
+    c->loss_cap = 4096;
+    SSB_ALLOC(c->loss, (size_t)c->loss_cap, sb);
+    SSB_ALLOC(c->flag, (size_t)1, sb);
+    c->g_bytes = gb;
+    c->scratch_bytes = sb;
+
+    // per-BF geometry (float64 on the host)
+    std::vector<float4> kgeo(c->n_bf);
+    std::vector<double2> kal(c->n_bf);
+    for (int k = 0; k < c->n_bf; ++k) {
+        const double ay = (double)g->bf_det_yx[2 * k] * c->dalpha;
+        const double ax = (double)g->bf_det_yx[2 * k + 1] * c->dalpha;
+        const double r = std::sqrt(ax * ax + ay * ay);
+        const double amp = std::min(1.0, std::max(0.0, (c->semi - r) / c->dalpha + 0.5));
+        kgeo[k] = make_float4((float)ax, (float)ay, (float)amp, 0.f);
+        kal[k] = make_double2(ax, ay);
+    }
+    std::vector<float2> tw(N);
+    for (int m = 0; m < N; ++m) {
+        const double a = 2.0 * M_PI * (double)m / (double)N;
+        tw[m] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+#define SSB_CK_BAIL(call)                                  \
+    if ((e = (call)) != cudaSuccess) {                     \
+        st = cuda_fail(e, #call);                          \
+        return bail(st);                                   \
+    }
+    SSB_CK_BAIL(cudaMemcpyAsync(c->kgeo, kgeo.data(), sizeof(float4) * c->n_bf, cudaMemcpyHostToDevice, s));
+    SSB_CK_BAIL(cudaMemcpyAsync(c->kalpha, kal.data(), sizeof(double2) * c->n_bf, cudaMemcpyHostToDevice, s));
+    SSB_CK_BAIL(cudaMemcpyAsync(c->tw, tw.data(), sizeof(float2) * N, cudaMemcpyHostToDevice, s));
+    SSB_CK_BAIL(cudaMemsetAsync(c->flag, 0, sizeof(int), s));
+
+    // counts -> float32 -> G, in chunks of BF planes
+    const size_t esz = dtype == SSB_U16 ? 2 : 4;
+    const size_t per_bf = P * esz + P * sizeof(float) + (size_t)H * N * sizeof(float2);
+    const int KC = (int)std::max<size_t>(1, std::min<size_t>((size_t)c->n_bf, (256u << 20) / per_bf));
+    void *raw = nullptr;
+    float *F = nullptr;
+    float2 *tmp = nullptr;
+    auto free_stage = [&]() {
+        if (raw) cudaFree(raw);
+        if (F) cudaFree(F);
+        if (tmp) cudaFree(tmp);
+        raw = nullptr;
+        F = nullptr;
+        tmp = nullptr;
+    };
+    if (!counts_on_device && (e = cudaMalloc(&raw, (size_t)KC * P * esz)) != cudaSuccess) {
+        free_stage();
+        return bail(cuda_fail(e, "cudaMalloc counts staging"));
+    }
+    if ((e = cudaMalloc((void **)&F, (size_t)KC * P * sizeof(float))) != cudaSuccess ||
+        (e = cudaMalloc((void **)&tmp, (size_t)KC * H * N * sizeof(float2))) != cudaSuccess) {
+        free_stage();
+        return bail(cuda_fail(e, "cudaMalloc prepare staging"));
+    }
+    for (int k0 = 0; k0 < c->n_bf; k0 += KC) {
+        const int kc = std::min(KC, c->n_bf - k0);
+        const char *src = (const char *)counts + (size_t)k0 * P * esz;
+        const void *dsrc = src;
+        if (!counts_on_device) {
+            if ((e = cudaMemcpyAsync(raw, src, (size_t)kc * P * esz, cudaMemcpyHostToDevice, s)) !=
+                cudaSuccess) {
+                free_stage();
+                return bail(cuda_fail(e, "counts host-to-device copy"));
+            }
+            dsrc = raw;
+        }
+        if ((e = launch_unpack(dsrc, dtype, (size_t)kc * P, F, c->flag, s)) != cudaSuccess ||
+            (e = launch_rfft2(N, F, tmp, c->G + (size_t)k0 * H * N, kc, c->tw, s)) != cudaSuccess) {
+            free_stage();
+            return bail(cuda_fail(e, "G cache build"));
+        }
+    }
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) {
+        free_stage();
+        return bail(cuda_fail(e, "prepare synchronise"));
+    }
+    free_stage();
+    if ((st = check_flag(c, s)) != SSB_OK) return bail(st);
+    *out = c;
+    return SSB_OK;
+#undef SSB_ALLOC
+#undef SSB_CK_BAIL
+}
+
+ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *loss_out,
+                          void *cuda_stream) {
+    g_last_error.clear();
+    if (!c || !theta || !loss_out) return fail(SSB_ERR_ARG, "NULL argument");
+    if (T < 1) return fail(SSB_ERR_ARG, "T must be >= 1");
+    for (int t = 0; t < T; ++t)
+        if (!valid_theta(theta[t])) return fail(SSB_ERR_ARG, "non-finite theta");
+    DeviceGuard dg(c->dev);
+    if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    const ObjectiveArgs a = c->args();
+    for (int t0 = 0; t0 < T; t0 += c->loss_cap) {
+        const int tn = std::min(c->loss_cap, T - t0);
+        for (int t = 0; t < tn; ++t) {
+            cudaError_t e = run_objective(a, theta[t0 + t], c->loss + t, false, s);
+            if (e != cudaSuccess) return cuda_fail(e, "objective launch");
+        }
+        SSB_CK(cudaMemcpyAsync(loss_out + t0, c->loss, sizeof(double) * tn, cudaMemcpyDeviceToHost, s));
+        SSB_CK(cudaStreamSynchronize(s));
+    }
+    return SSB_OK;
+}
+
+ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phase_out,
+                           float *object_c64_out, double *loss_out, void *cuda_stream) {
+    g_last_error.clear();
+    if (!c || !theta || !mean_phase_out) return fail(SSB_ERR_ARG, "NULL argument");
+    if (!valid_theta(*theta)) return fail(SSB_ERR_ARG, "non-finite theta");
+    DeviceGuard dg(c->dev);
+    if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    const ObjectiveArgs a = c->args();
+    cudaError_t e = run_objective(a, *theta, c->loss, object_c64_out != nullptr, s);
+    if (e != cudaSuccess) return cuda_fail(e, "objective launch");
+    if ((e = launch_finalize(a, mean_phase_out, object_c64_out, s)) != cudaSuccess)
+        return cuda_fail(e, "finalize launch");
+    if (loss_out) {
+        SSB_CK(cudaMemcpyAsync(loss_out, c->loss, sizeof(double), cudaMemcpyDeviceToHost, s));
+    }
+    SSB_CK(cudaStreamSynchronize(s));
+    return SSB_OK;
+}
+
+ssb_status ssb_info(const ssb_ctx *c, size_t *g_bytes, size_t *scratch_bytes) {
+    if (!c) return fail(SSB_ERR_ARG, "NULL context");
+    if (g_bytes) *g_bytes = c->g_bytes;
+    if (scratch_bytes) *scratch_bytes = c->scratch_bytes;
+    return SSB_OK;
+}
+
+ssb_status ssb_export_g(const ssb_ctx *c, void *dst, int dst_on_device, void *cuda_stream) {
+    g_last_error.clear();
+    if (!c || !dst) return fail(SSB_ERR_ARG, "NULL argument");
+    DeviceGuard dg(c->dev);
+    if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    SSB_CK(cudaMemcpyAsync(dst, c->G, c->g_bytes,
+                           dst_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, s));
+    SSB_CK(cudaStreamSynchronize(s));
+    return SSB_OK;
+}
+
+ssb_status ssb_unpack_counts(const void *in_device, ssb_dtype dtype, size_t n, float *out_device,
+                             void *cuda_stream) {
+    g_last_error.clear();
+    if ((!in_device || !out_device) && n > 0) return fail(SSB_ERR_ARG, "NULL argument");
+    if (dtype != SSB_U16 && dtype != SSB_U32) return fail(SSB_ERR_ARG, "unknown dtype");
+    if (n == 0) return SSB_OK;
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    int *flag = nullptr;
+    SSB_CK(cudaMalloc((void **)&flag, sizeof(int)));
+    cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = launch_unpack(in_device, dtype, n, out_device, flag, s);
+    int h = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h, flag, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(flag);
+    if (e != cudaSuccess) return cuda_fail(e, "unpack");
+    if (h & 1) return fail(SSB_ERR_ARG, "a count exceeds 2^24 and cannot be converted to float32 exactly");
+    return SSB_OK;
+}
+
+void ssb_destroy(ssb_ctx *c) {
+    if (!c) return;
+    DeviceGuard dg(c->dev);
+    cudaDeviceSynchronize();
+    free_ctx(c);
+}
+
+}  // extern "C"

@@ -1,0 +1,147 @@
+// Device building blocks shared by the SSB kernels: complex helpers, a batched
+// shared-memory Stockham FFT and the per-element SSB correction factor.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssb {
+
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+    return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.x, b.y, a.y * b.x));
+}
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+__device__ __forceinline__ float2 cconj(float2 a) { return make_float2(a.x, -a.y); }
+
+// Twiddle exp(S * 2 pi i m / N) from a table tw[m] = exp(+2 pi i m / N), 0 <= m < N.
+template <int S>
+__device__ __forceinline__ float2 twid(const float2 *tw, int m) {
+    float2 w = tw[m];
+    return S > 0 ? w : cconj(w);
+}
+
+// In-place 4-point DFT with exponent sign S (+1 inverse, -1 forward).
+template <int S>
+__device__ __forceinline__ void dft4(float2 &a0, float2 &a1, float2 &a2, float2 &a3) {
+    float2 t0 = cadd(a0, a2), t1 = csub(a0, a2), t2 = cadd(a1, a3), d = csub(a1, a3);
+    float2 t3 = S > 0 ? make_float2(-d.y, d.x) : make_float2(d.y, -d.x);  // (i S) d
+    a0 = cadd(t0, t2);
+    a2 = csub(t0, t2);
+    a1 = cadd(t1, t3);
+    a3 = csub(t1, t3);
+}
+
+// NF length-N transforms held in shared memory at buf0 + f * LD (f < NF), computed by
+// all nthr threads of the block with a Stockham autosort schedule: radix-4 passes, then
+// one radix-2 pass when log2 N is odd.  Pass with span Ns and radix R: butterfly j
+// reads x[j + r N/R], applies exp(S 2 pi i r (j mod Ns)/(Ns R)), takes the R-point DFT
+// and writes y[(j - j mod Ns) R + j mod Ns + r Ns] (Stockham's self-sorting FFT, as in
+// Govindaraju et al., "High performance discrete Fourier transforms on graphics
+// processors", SC 2008).  Unnormalised.  Returns 0 if the result is in buf0, 1 if in buf1.
+// Every thread of the block must call it (it synchronises the block after each pass).
+template <int N, int S>
+__device__ int fft_batch_smem(float2 *buf0, float2 *buf1, int NF, int LD, const float2 *tw,
+                              int tid, int nthr) {
+    float2 *src = buf0, *dst = buf1;
+    int which = 0;
+    int Ns = 1;
+#pragma unroll 1
+    for (; Ns * 4 <= N; Ns *= 4) {
+        constexpr int nb = N / 4;
+        const int step = N / (Ns * 4);
+        for (int idx = tid; idx < NF * nb; idx += nthr) {
+            const int f = idx / nb, j = idx - f * nb;
+            const float2 *s = src + f * LD;
+            float2 *d = dst + f * LD;
+            const int k = j & (Ns - 1);
+            float2 v0 = s[j], v1 = s[j + nb], v2 = s[j + 2 * nb], v3 = s[j + 3 * nb];
+            if (Ns > 1) {
+                const int m = k * step;
+                v1 = cmul(v1, twid<S>(tw, m));
+                v2 = cmul(v2, twid<S>(tw, 2 * m));
+                v3 = cmul(v3, twid<S>(tw, 3 * m));
+            }
+            dft4<S>(v0, v1, v2, v3);
+            const int o = (j - k) * 4 + k;
+            d[o] = v0;
+            d[o + Ns] = v1;
+            d[o + 2 * Ns] = v2;
+            d[o + 3 * Ns] = v3;
+        }
+        __syncthreads();
+        float2 *t = src; src = dst; dst = t;
+        which ^= 1;
+    }
+    if (Ns < N) {  // radix-2 pass, Ns == N/2
+        constexpr int nb = N / 2;
+        for (int idx = tid; idx < NF * nb; idx += nthr) {
+            const int f = idx / nb, j = idx - f * nb;
+            const float2 *s = src + f * LD;
+            float2 *d = dst + f * LD;
+            float2 v0 = s[j], v1 = cmul(s[j + nb], twid<S>(tw, j));
+            d[j] = cadd(v0, v1);
+            d[j + nb] = csub(v0, v1);
+        }
+        __syncthreads();
+        which ^= 1;
+    }
+    return which;
+}
+
+// fftfreq ordering: bins 0..N/2-1 are non-negative, N/2..N-1 negative (Nyquist negative).
+template <int N>
+__device__ __forceinline__ int signed_bin(int q) { return q < N / 2 ? q : q - N; }
+
+// Per-trial constants of the correction (float32 copies of host float64 values).
+struct TrialConst {
+    float cr, sr;       // cos, sin of the scan rotation
+    float lam;          // wavelength (Angstrom)
+    float inv_nstep;    // 1 / (N * scan step)  (1/Angstrom per frequency bin)
+    float semi;         // aperture semiangle (rad)
+    float inv_dalpha;   // 1 / detector sampling (1/rad)
+    int mode;           // 0 = SSB2, 1 = SSB1
+};
+
+__device__ __forceinline__ float soft_aperture(float ax, float ay, float semi, float inv_da) {
+    const float r = sqrtf(fmaf(ax, ax, ay * ay));
+    return fminf(fmaxf(fmaf(semi - r, inv_da, 0.5f), 0.0f), 1.0f);
+}
+
+// Correction factor F_k(Q) such that C_k(Q) = G_k(Q) F_k(Q).
+//
+// With chi quadratic, chi(alpha_k -+ lambda Q') = chi(alpha_k) + chi(lambda Q') -+ B with
+// B = 2 pi alpha_k^T M Q' linear in Q (M the aberration matrix), so
+//   Gamma_k = a_k e^{-iB} [a_- e^{i chiQ} - a_+ e^{-i chiQ}] = a_k e^{-iB} D,
+//   D = (a_- - a_+) cos chiQ + i (a_- + a_+) sin chiQ,
+// and conj(Gamma)/|Gamma| = e^{iB} conj(D)/|D| (an exact rewriting).  chiQ comes from the
+// per-trial table E = e^{i chiQ}; B is carried exactly as a 32-bit fixed-point fraction of
+// a turn, b_x sx + b_y sy mod 2^32, so its range reduction is exact.
+// SSB1: F = e^{i(chi(alpha_k) - chi(alpha_k - lambda Q'))} = e^{iB} conj(E), masked by
+// a_k a_- > 0.  F(0) = 1 (the DC term is kept).  geo = (alpha_x, alpha_y, a_k, -).
+template <int N>
+__device__ __forceinline__ float2 correction_factor(int ny, int nx, float4 geo, uint2 bturn,
+                                                    float2 e, const TrialConst &tc) {
+    if ((nx | ny) == 0) return make_float2(1.0f, 0.0f);
+    if (!(geo.z > 0.0f)) return make_float2(0.0f, 0.0f);
+    const int sx = signed_bin<N>(nx), sy = signed_bin<N>(ny);
+    const float fx = (float)sx * tc.inv_nstep, fy = (float)sy * tc.inv_nstep;
+    const float lx = tc.lam * fmaf(tc.cr, fx, -tc.sr * fy);
+    const float ly = tc.lam * fmaf(tc.sr, fx, tc.cr * fy);
+    const float am = soft_aperture(geo.x - lx, geo.y - ly, tc.semi, tc.inv_dalpha);
+    const uint32_t ph = bturn.x * (uint32_t)sx + bturn.y * (uint32_t)sy;
+    float sb, cb;
+    sincospif((float)(int32_t)ph * 4.656612873077393e-10f, &sb, &cb);  // 2 pi ph / 2^32
+    if (tc.mode == 1) {
+        if (!(am > 0.0f)) return make_float2(0.0f, 0.0f);
+        return cmul(make_float2(cb, sb), cconj(e));
+    }
+    const float ap = soft_aperture(geo.x + lx, geo.y + ly, tc.semi, tc.inv_dalpha);
+    const float dx = (am - ap) * e.x, dy = (am + ap) * e.y;
+    const float d2 = fmaf(dx, dx, dy * dy);
+    if (!(d2 > 0.0f)) return make_float2(0.0f, 0.0f);
+    const float inv = rsqrtf(d2);
+    return cmul(make_float2(dx * inv, -dy * inv), make_float2(cb, sb));
+}
+
+}  // namespace ssb

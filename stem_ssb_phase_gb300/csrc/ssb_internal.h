@@ -1,0 +1,55 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ssb.h"
+
+namespace ssb {
+
+// Launch-count bookkeeping (every kernel launch of the library goes through this).
+void count_launch(uint64_t n = 1);
+
+// Per-trial float64 constants derived on the host from theta and the geometry.
+struct TrialHost {
+    double cr, sr;        // rotation cos / sin
+    double m00, m01, m11; // aberration matrix M (Angstrom): chi(u) = (pi/lambda) u^T M u
+};
+
+// ---- G-cache builder (ssb_prep.cu) ----
+// counts [kc][N][N] raw (dtype) -> float32 F [kc][N][N]; sets *flag bit 1 on counts > 2^24
+cudaError_t launch_unpack(const void *raw, ssb_dtype dtype, size_t n, float *out, int *flag,
+                          cudaStream_t s);
+// F [kc][N][N] float32 -> G [kc][N/2+1][N] complex64 using tmp [kc][N/2+1][N]
+cudaError_t launch_rfft2(int N, const float *F, float2 *tmp, float2 *G, int kc,
+                         const float2 *tw, cudaStream_t s);
+
+// ---- objective (ssb_objective.cu) ----
+struct ObjectiveArgs {
+    int N;
+    int n_bf;
+    const float2 *G;        // [n_bf][N/2+1][N]
+    const float4 *kgeo;     // [n_bf] (alpha_x, alpha_y, a_k, 0), float32
+    const double2 *kalpha;  // [n_bf] (alpha_x, alpha_y), float64
+    uint2 *kturn;           // [n_bf] per-trial B slopes (32-bit turn fractions)
+    float2 *E;              // [N][N] per-trial e^{i chi(lambda Q')}
+    const float2 *tw;       // [N] twiddles exp(+2 pi i m/N)
+    float2 *X;              // [B][N][N] column-pass intermediate
+    int B;                  // BF batch
+    double *S1, *S2;        // [N][N] float64 accumulators
+    double2 *Osum;          // [N][N] float64 object accumulator (nullable)
+    double *loss;           // device float64, one per trial slot
+    int mode;               // 0 SSB2, 1 SSB1
+    double step, lam, semi, dalpha;  // geometry (Angstrom, rad)
+};
+
+// Run one full objective evaluation (S1/S2 zeroed first), loss written to *loss_slot.
+cudaError_t run_objective(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,
+                          bool want_object, cudaStream_t s);
+// mean phase = S1/n_bf (float32), object = Osum * scale (complex64) if out_obj != nullptr
+cudaError_t launch_finalize(const ObjectiveArgs &a, float *mean_phase, float *out_obj,
+                            cudaStream_t s);
+
+}  // namespace ssb

@@ -1,0 +1,77 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports every symbol the
+public header declares; the binding rejects bad arguments before reaching a kernel."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import stem_ssb_phase_gb300 as ssbgpu
+from stem_ssb_phase_gb300 import build as ssbbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "ssb.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ssbbuild.build()
+    return ssbgpu.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssb_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert set(declared_functions()) == set(ssbgpu.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in ssbgpu.STATUS.items():
+        assert ssbgpu.status_string(code) == name
+
+
+def test_null_arguments_fail_before_any_device_work(lib):
+    out = ctypes.c_void_p()
+    assert lib.ssb_prepare(None, None, 0, 0, 0, None, ctypes.byref(out)) == 1
+    assert out.value is None
+    assert lib.ssb_loss_batch(None, None, 1, None, None) == 1
+    assert lib.ssb_reconstruct(None, None, None, None, None, None) == 1
+    assert lib.ssb_info(None, None, None) == 1
+    assert lib.ssb_export_g(None, None, 0, None) == 1
+
+
+def test_unsupported_scan_size_is_rejected_on_the_host(lib):
+    yx = np.zeros((1, 2), np.float32)
+    g = ssbgpu._Geometry(48, 0.25, 0.0197, 20.0, 3.3, 1,
+                         yx.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    counts = np.zeros((1, 48, 48), np.uint16)
+    out = ctypes.c_void_p()
+    st = lib.ssb_prepare(ctypes.byref(g), counts.ctypes.data, 0, 0, 0, None, ctypes.byref(out))
+    assert st == 2  # SSB_ERR_UNSUPPORTED
+    assert b"scan_n" in lib.ssb_last_error()
+
+
+@pytest.mark.parametrize("field,value", [("scan_step_A", float("nan")), ("wavelength_A", -1.0),
+                                         ("n_bf", 0)])
+def test_invalid_geometry_is_rejected(lib, field, value):
+    yx = np.zeros((1, 2), np.float32)
+    vals = dict(scan_n=32, scan_step_A=0.25, wavelength_A=0.0197, semiangle_mrad=20.0,
+                det_sampling_mrad=3.3, n_bf=1)
+    vals[field] = value
+    g = ssbgpu._Geometry(vals["scan_n"], vals["scan_step_A"], vals["wavelength_A"],
+                         vals["semiangle_mrad"], vals["det_sampling_mrad"], vals["n_bf"],
+                         yx.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    counts = np.zeros((1, 32, 32), np.uint16)
+    out = ctypes.c_void_p()
+    assert lib.ssb_prepare(ctypes.byref(g), counts.ctypes.data, 0, 0, 0, None,
+                           ctypes.byref(out)) == 1
