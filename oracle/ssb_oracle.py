@@ -37,7 +37,12 @@ Readings where the pages are silent (each listed in the design notes):
     lambda Q') > 0; "identity" (C = G) is a test mode only;
   * chi(alpha) = (pi/lambda)[C10 |alpha|^2 + C12((ax^2 - ay^2) cos 2phi12
     + 2 ax ay sin 2phi12)], C in Angstrom (nm x 10), alpha in rad;
-  * a(alpha) = clip((alpha_c - |alpha|)/d_alpha + 1/2, 0, 1);
+  * a(alpha) = clip((alpha_c - |alpha|)/d_alpha + 1/2, 0, 1), taken as exactly 0 when
+    that value is below APERTURE_FLOOR = 2^-16.  A scan grid commensurate with the
+    detector (e.g. no rotation) places shifted apertures exactly on the outer edge, where
+    unit-modulus normalisation turns "zero transfer" into a full-magnitude term; without
+    the floor, rounding alone would decide between the two.  The pages' zero-transfer
+    rule ("both shifted apertures are exactly zero") is read with this floor;
   * Q' = R_theta Q with Q'x = cos Qx - sin Qy, Q'y = sin Qx + cos Qy; the detector
     angles are not rotated;
   * the Nyquist bin of fftfreq is negative and the correction is evaluated at the
@@ -53,6 +58,7 @@ from typing import Optional, Sequence
 import numpy as np
 
 MODES = ("ssb2", "ssb1", "identity")
+APERTURE_FLOOR = 2.0 ** -16
 
 
 # ----------------------------------------------------------------------------
@@ -81,9 +87,11 @@ class Geom:
 
 
 def aperture(ax, ay, semi, dalpha):
-    """Soft probe aperture a(alpha) = clip((alpha_c - |alpha|)/d_alpha + 1/2, 0, 1)."""
+    """Soft probe aperture a(alpha) = clip((alpha_c - |alpha|)/d_alpha + 1/2, 0, 1),
+    with values below APERTURE_FLOOR taken as exactly zero."""
     r = np.sqrt(ax * ax + ay * ay)
-    return np.clip((semi - r) / dalpha + 0.5, 0.0, 1.0)
+    a = np.clip((semi - r) / dalpha + 0.5, 0.0, 1.0)
+    return np.where(a < APERTURE_FLOOR, 0.0, a)
 
 
 def chi(ax, ay, lam, c10_A, c12_A, phi12):

@@ -225,7 +225,8 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
         const double ay = (double)g->bf_det_yx[2 * k] * c->dalpha;
         const double ax = (double)g->bf_det_yx[2 * k + 1] * c->dalpha;
         const double r = std::sqrt(ax * ax + ay * ay);
-        const double amp = std::min(1.0, std::max(0.0, (c->semi - r) / c->dalpha + 0.5));
+        double amp = std::min(1.0, std::max(0.0, (c->semi - r) / c->dalpha + 0.5));
+        if (amp < 1.0 / 65536.0) amp = 0.0;  // zero-transfer floor of the aperture
         kgeo[k] = make_float4((float)ax, (float)ay, (float)amp, 0.f);
         kal[k] = make_double2(ax, ay);
     }

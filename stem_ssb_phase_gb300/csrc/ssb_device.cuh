@@ -103,9 +103,15 @@ struct TrialConst {
     int mode;           // 0 = SSB2, 1 = SSB1
 };
 
+// Amplitudes below this are exactly zero transfer: a scan grid commensurate with the
+// detector can put a shifted aperture exactly on its outer edge, where the unit-modulus
+// normalisation would otherwise let rounding choose between zero and a full-size term.
+constexpr float kApertureFloor = 1.0f / 65536.0f;
+
 __device__ __forceinline__ float soft_aperture(float ax, float ay, float semi, float inv_da) {
     const float r = sqrtf(fmaf(ax, ax, ay * ay));
-    return fminf(fmaxf(fmaf(semi - r, inv_da, 0.5f), 0.0f), 1.0f);
+    const float a = fminf(fmaxf(fmaf(semi - r, inv_da, 0.5f), 0.0f), 1.0f);
+    return a < kApertureFloor ? 0.0f : a;
 }
 
 // Correction factor F_k(Q) such that C_k(Q) = G_k(Q) F_k(Q).

@@ -16,6 +16,8 @@ def _signed(q, n):
 
 def _probe(ax, ay, lam, semi, da, c10, c12, phi12):
     amp = min(1.0, max(0.0, (semi - math.hypot(ax, ay)) / da + 0.5))
+    if amp < 2.0 ** -16:  # zero-transfer floor of the aperture
+        amp = 0.0
     ph = (math.pi / lam) * (c10 * (ax * ax + ay * ay)
                             + c12 * ((ax * ax - ay * ay) * math.cos(2 * phi12)
                                      + 2 * ax * ay * math.sin(2 * phi12)))
