@@ -1,0 +1,361 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact SSB phase-variance objective on GB300.
+
+One step = one ssb_loss_batch call over T trials (default T = 1: one exact objective)
+on the full workload: 512 x 512 scan, 192 x 192 detector, 8,937 BF pixels, packed
+uint32 Poisson counts (mean 1,000), complex64 Hermitian G cache of 9.41 GB resident in
+HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--trials T]
+
+Metric: exact BF x scan samples per second (n_bf * N^2 * T per step), with ms per step.
+--impl reference times the float64 CPU oracle on a bounded BF sample of the same
+workload on the host cores.  Under torchrun each rank runs an independent replica
+(the objective is evaluated whole on each GPU; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import ssb_synth  # noqa: E402
+
+METRIC = "exact BF×scan samples/s; ms per SSB objective at 512² scan, 8,937 BF"
+UNIT = "BF×scan samples/s"
+# Apple M5 native Metal, full 512^2 x 8,937-BF objective, best p50 after the fftA blocks
+# ("Later SSB performance checkpoints", fftA intermediate section): 221.6 ms.
+PAGES_MS = 221.6
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for _, _, r in rows for j in range(4) if r[j].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- roofline helpers
+
+def _algorithmic_bytes(n_bf: int, n: int) -> dict:
+    """Bytes each kernel must move per objective, by kernel name (the G cache read once;
+    the column-pass intermediate written once and read once where a kernel boundary
+    separates the passes; float64 moment accumulators read and written per BF batch are
+    not counted)."""
+    h = n // 2 + 1
+    g = n_bf * h * n * 8
+    x = n_bf * n * n * 8
+    return {"k_correct_cols": g + x, "k_rows_moments": x}
+
+
+def _traffic_record():
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return {}
+    with open(p) as f:
+        return json.load(f)
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "stem_ssb_phase_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+
+def cpu_oracle_run(geom, counts_sample, theta, workers: int):
+    import oracle
+    t0 = time.perf_counter()
+    res = oracle.objective(geom, theta, counts=counts_sample, workers=workers,
+                           bf_range=(0, counts_sample.shape[0]))
+    return time.perf_counter() - t0, res["loss"]
+
+
+def cpu_sample_size(n_bf: int, cores: int, per_bf_s: float, target_s: float = 15.0) -> int:
+    return int(max(cores, min(n_bf, round(target_s * cores / max(per_bf_s, 1e-3)))))
+
+
+# ---------------------------------------------------------------- arms
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import stem_ssb_phase_gb300 as ssbgpu
+    from stem_ssb_phase_gb300 import build as _build
+
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.set_device(local_rank)
+    w = ssb_synth.WORKLOADS[args.workload]
+    geom, counts, _ = ssb_synth.simulate_counts_torch(w, "cuda")
+    n = geom.scan_n
+    cores = len(os.sched_getaffinity(0))
+    sample = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = counts[: min(geom.n_bf, 16 * cores * 4)].cpu().numpy()
+        sample = sample.view(np.uint32) if w.dtype == "u32" else sample.view(np.uint16)
+    ctx = ssbgpu.SSB(geom, counts)
+    del counts
+    torch.cuda.empty_cache()
+    thetas = ssb_synth.draw_trials(w, args.trials)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        ctx.loss_batch(thetas)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: inputs resident in HBM
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    l0 = ssbgpu.kernel_launches()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        losses = ctx.loss_batch(thetas)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = ssbgpu.kernel_launches() - l0
+    t_dev = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        tt = torch.tensor([t_dev], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_dev = float(tt.item())
+    units = geom.n_bf * n * n * args.trials
+    value = world * args.steps * units / t_dev
+    ms_per_step = 1e3 * t_dev / args.steps
+
+    # ---- end to end through the public API: host theta in, host losses out
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    h0 = time.perf_counter()
+    for _ in range(args.steps):
+        ctx.loss_batch(thetas)
+    t_e2e = time.perf_counter() - h0
+    if world > 1:
+        tt = torch.tensor([t_e2e], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e = {"value": world * args.steps * units / t_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": 32 * args.trials, "d2h_bytes_per_step": 8 * args.trials}
+
+    # ---- per-kernel device times of one objective (events on the library's stream)
+    prof = ctx.profile(thetas[0])
+    peak, peak_kind = _peaks()
+    algo = _algorithmic_bytes(geom.n_bf, n)
+    top = max(prof.items(), key=lambda kv: kv[1][1])
+    name, (nl, ms) = top
+    total_ms = sum(v[1] for v in prof.values())
+    roof = None
+    if name in algo:
+        per_launch = algo[name] / nl
+        achieved = per_launch / (ms / nl / 1e3) / 1e9
+        rec = _traffic_record().get(name)
+        traffic = None
+        if rec and rec.get("source") == source_digest():
+            traffic = rec.get("bytes_per_launch")
+        roof = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "algorithmic_bytes_per_launch": int(per_launch),
+                "peak_kind": peak_kind, "launches_per_objective": nl,
+                "kernel_share": round(ms / total_ms, 3)}
+    objective_bytes = geom.n_bf * (n // 2 + 1) * n * 8
+    hbm_g_only = objective_bytes / (ms_per_step / 1e3 / args.trials) / 1e9
+
+    cpu = None
+    if sample is not None:
+        import oracle
+        per_bf, _ = cpu_oracle_run(geom, sample[:1], thetas[0], workers=1)
+        s = min(sample.shape[0], cpu_sample_size(geom.n_bf, cores, per_bf))
+        t_cpu, _ = cpu_oracle_run(geom, sample[:s], thetas[0], workers=cores)
+        cpu = {"value": s * n * n / t_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "%d of %d BF pixels of the same workload, one trial, float64 NumPy "
+                         "oracle in %d spawned processes (%.1f s)" % (s, geom.n_bf, cores, t_cpu)}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / (2342780928 / (PAGES_MS / 1e3)) if args.workload == "full" else None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "%s: %dx%d scan, %dx%d detector, %d BF, %s counts (mean %g), "
+                                   "complex64 Hermitian G cache %.2f GB" % (
+                                       w.name, n, n, w.det_n, w.det_n, geom.n_bf, w.dtype,
+                                       w.mean_count, objective_bytes / 1e9),
+                       "trials_per_step": args.trials, "transfer": "ssb2",
+                       "l2": "inputs (G cache %.1f GB) exceed the 129 MB L2; no flush" % (objective_bytes / 1e9),
+                       "parallelism": "replicas x%d" % world},
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "roofline": roof,
+            "hbm_fraction_g_only": round(hbm_g_only / peak, 4),
+            "kernel_ms_per_objective": {k: round(v[1], 4) for k, v in prof.items()},
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "loss_check": float(losses[0]),
+        }
+        print(json.dumps(out), flush=True)
+    ctx.close()
+
+
+def run_reference(args, rank, world):
+    """The float64 CPU oracle on a bounded BF sample of the same workload."""
+    if rank != 0:
+        return
+    w = ssb_synth.WORKLOADS[args.workload]
+    cores = len(os.sched_getaffinity(0))
+    full = ssb_synth.make_geometry(w)
+    n = full.scan_n
+    s = min(full.n_bf, 8 * cores)
+    idx = np.linspace(0, full.n_bf - 1, s).astype(int)
+    geom = ssb_synth.make_geometry(w, bf_subset=idx)
+    _, counts, _ = ssb_synth.simulate_counts_numpy(w, geom=geom)
+    theta = ssb_synth.draw_trials(w, 1)[0]
+    for _ in range(args.warmup):
+        cpu_oracle_run(geom, counts, theta, workers=cores)
+    times = []
+    for _ in range(args.steps):
+        t, loss = cpu_oracle_run(geom, counts, theta, workers=cores)
+        times.append(t)
+    tot = sum(times)
+    value = args.steps * s * n * n / tot
+    sample = ("%d of %d BF pixels (evenly spaced) of the same workload per step, one trial, "
+              "float64 NumPy oracle in %d spawned processes" % (s, full.n_bf, cores))
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": value / (2342780928 / (PAGES_MS / 1e3)) if args.workload == "full" else None,
+           "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "%s (BF sample)" % w.name, "bf_sample": s, "trials_per_step": 1},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "loss_check": loss}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--trials", type=int, default=1)
+    ap.add_argument("--workload", default="full", choices=sorted(ssb_synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local_rank = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -119,6 +119,20 @@ ssb_status ssb_export_g(const ssb_ctx *c, void *dst, int dst_on_device, void *cu
 ssb_status ssb_unpack_counts(const void *in_device, ssb_dtype dtype, size_t n,
                              float *out_device, void *cuda_stream);
 
+/* Per-kernel timing of one objective evaluation (tracing aid, as the pages' stage
+ * profiles): the call runs one exact objective at theta with a CUDA event pair around
+ * every launch on cuda_stream, then reports, per kernel name, the launch count and the
+ * summed device time in milliseconds.  out: host [cap]; *n_out receives the number of
+ * distinct kernels (entries beyond cap are dropped).  Synchronises the stream. */
+typedef struct {
+    char   name[48];
+    int    launches;
+    double ms;
+} ssb_kernel_time;
+
+ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel_time *out,
+                                 int cap, int *n_out, void *cuda_stream);
+
 /* Human-readable name of a status. */
 const char *ssb_status_string(ssb_status s);
 

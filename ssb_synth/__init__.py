@@ -190,53 +190,51 @@ def simulate_counts_torch(w: Workload, device, geom: Optional[Geometry] = None,
     phi = object_phase(n, w.object_sigma_px, w.object_rms_rad, rng)
     dev = torch.device(device)
     tf = torch.fft.fft2(torch.exp(1j * torch.from_numpy(phi).to(dev)))  # complex128
-    tf64 = tf
+    tf2 = (tf.abs() ** 2).to(torch.float32)[None]
     tf = tf.to(torch.complex64)
-    f = torch.fft.fftfreq(n, d=geom.scan_step_A, device=dev, dtype=torch.float64)
+    f = np.fft.fftfreq(n, d=geom.scan_step_A)
     qx, qy = f[None, :], f[:, None]
     c, s = math.cos(truth[3]), math.sin(truth[3])
     lam = geom.wavelength_A
-    lqx = (lam * (c * qx - s * qy))
-    lqy = (lam * (s * qx + c * qy))
+    lqx = torch.from_numpy(lam * (c * qx - s * qy)).to(dev, torch.float32)
+    lqy = torch.from_numpy(lam * (s * qx + c * qy)).to(dev, torch.float32)
     semi = geom.semiangle_mrad * 1e-3
     da = geom.det_sampling_mrad * 1e-3
     c10, c12, phi12 = truth[0] * 10.0, truth[1] * 10.0, truth[2]
-    ak = torch.from_numpy(geom.bf_det_yx.astype(np.float64) * da).to(dev)
+    ak = torch.from_numpy(geom.bf_det_yx.astype(np.float64) * da).to(dev, torch.float32)
+    k_pi = math.pi / lam
+    c2, s2 = math.cos(2 * phi12), math.sin(2 * phi12)
 
     def probe(kk):
+        # float32 is ample for synthesising inputs; phases are reduced mod 2 pi
         ax = ak[kk, 1][:, None, None] - lqx[None]
         ay = ak[kk, 0][:, None, None] - lqy[None]
         r = torch.sqrt(ax * ax + ay * ay)
         amp = torch.clamp((semi - r) / da + 0.5, 0.0, 1.0)
-        ph = (math.pi / lam) * (c10 * (ax * ax + ay * ay)
-                                + c12 * ((ax * ax - ay * ay) * math.cos(2 * phi12)
-                                         + 2.0 * ax * ay * math.sin(2 * phi12)))
-        return amp, ph
+        ph = k_pi * (c10 * (ax * ax + ay * ay) + c12 * ((ax * ax - ay * ay) * c2 + 2.0 * ax * ay * s2))
+        return amp, torch.remainder(ph, 2 * math.pi)
 
-    tf2 = (tf64.abs() ** 2)[None]
     means = []
     for k0 in range(0, geom.n_bf, chunk):
         kk = torch.arange(k0, min(geom.n_bf, k0 + chunk), device=dev)
         amp, _ = probe(kk)
-        means.append(((tf2 * amp * amp).sum(dim=(1, 2)) / float(n) ** 4))
+        means.append(((tf2 * amp * amp).sum(dim=(1, 2), dtype=torch.float64) / float(n) ** 4))
     scale = w.mean_count / float(torch.cat(means).mean())
     tdt = torch.int32 if w.dtype == "u32" else torch.int16
-    maxv = 2 ** 32 - 1 if w.dtype == "u32" else 2 ** 16 - 1
     counts = torch.empty((geom.n_bf, n, n), dtype=tdt, device=dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(w.seed)
     for k0 in range(0, geom.n_bf, chunk):
         kk = torch.arange(k0, min(geom.n_bf, k0 + chunk), device=dev)
         amp, ph = probe(kk)
-        pk = torch.polar(amp.to(torch.float32), torch.remainder(ph, 2 * math.pi).to(torch.float32))
-        psi = torch.fft.ifft2(tf[None] * pk)
+        psi = torch.fft.ifft2(tf[None] * torch.polar(amp, ph))
         rate = (psi.real ** 2 + psi.imag ** 2) * scale
-        draw = torch.poisson(rate, generator=gen).clamp_(max=min(maxv, 2 ** 31 - 1))
+        draw = torch.poisson(rate, generator=gen)
         if w.dtype == "u32":
-            counts[k0:k0 + kk.numel()] = draw.to(torch.int64).to(torch.int32)
+            counts[k0:k0 + kk.numel()] = draw.clamp_(max=2 ** 31 - 1).to(torch.int32)
         else:
-            # store the uint16 bit pattern in an int16 tensor
-            counts[k0:k0 + kk.numel()] = draw.to(torch.int32).to(torch.int16)
+            # uint16 bit pattern stored in an int16 tensor
+            counts[k0:k0 + kk.numel()] = draw.clamp_(max=2 ** 16 - 1).to(torch.int32).to(torch.int16)
     return geom, counts, phi
 
 

@@ -22,8 +22,8 @@ STATUS = {0: "SSB_OK", 1: "SSB_ERR_ARG", 2: "SSB_ERR_UNSUPPORTED", 3: "SSB_ERR_O
 
 # every symbol include/ssb.h declares
 EXPORTS = ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_info", "ssb_export_g",
-           "ssb_unpack_counts", "ssb_status_string", "ssb_last_error", "ssb_kernel_launches",
-           "ssb_destroy")
+           "ssb_unpack_counts", "ssb_profile_objective", "ssb_status_string", "ssb_last_error",
+           "ssb_kernel_launches", "ssb_destroy")
 
 
 class SSBError(RuntimeError):
@@ -37,6 +37,10 @@ class _Geometry(ctypes.Structure):
                 ("wavelength_A", ctypes.c_double), ("semiangle_mrad", ctypes.c_double),
                 ("det_sampling_mrad", ctypes.c_double), ("n_bf", ctypes.c_int),
                 ("bf_det_yx", ctypes.POINTER(ctypes.c_float))]
+
+
+class _KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("ms", ctypes.c_double)]
 
 
 class _Params(ctypes.Structure):
@@ -63,6 +67,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_info.argtypes = [vp, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.ssb_export_g.argtypes = [vp, vp, i, vp]
     lib.ssb_unpack_counts.argtypes = [vp, i, sz, vp, vp]
+    lib.ssb_profile_objective.argtypes = [vp, ctypes.POINTER(_Params), ctypes.POINTER(_KernelTime),
+                                          i, ctypes.POINTER(i), vp]
     lib.ssb_status_string.argtypes = [i]
     lib.ssb_status_string.restype = ctypes.c_char_p
     lib.ssb_last_error.argtypes = []
@@ -72,7 +78,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_destroy.argtypes = [vp]
     lib.ssb_destroy.restype = None
     for name in ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_info",
-                 "ssb_export_g", "ssb_unpack_counts"):
+                 "ssb_export_g", "ssb_unpack_counts", "ssb_profile_objective"):
         getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -185,6 +191,17 @@ class SSB:
                                          ctypes.byref(loss) if want_loss else None,
                                          _stream_handle(stream)), "ssb_reconstruct")
         return mp, obj, (float(loss.value) if want_loss else None)
+
+    def profile(self, theta, stream=None) -> dict:
+        """{kernel name: (launches, total device ms)} for one objective at theta."""
+        cap = 64
+        out = (_KernelTime * cap)()
+        n = ctypes.c_int(0)
+        _check(self._lib.ssb_profile_objective(self._ctx, _params([theta]), out, cap,
+                                               ctypes.byref(n), _stream_handle(stream)),
+               "ssb_profile_objective")
+        return {out[j].name.decode(): (int(out[j].launches), float(out[j].ms))
+                for j in range(min(cap, n.value))}
 
     def export_g(self, stream=None):
         """The G cache as a CUDA complex64 tensor [n_bf][N/2+1][N] (Qx-major, Qy contiguous)."""

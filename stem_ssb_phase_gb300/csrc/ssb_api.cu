@@ -18,6 +18,34 @@ void count_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxe
 
 static thread_local std::string g_last_error;
 
+// ---- per-launch profiler (active only inside ssb_profile_objective) ----
+struct ProfRecord {
+    std::string name;
+    cudaEvent_t a, b;
+};
+struct Profiler {
+    std::vector<ProfRecord> recs;
+    bool open = false;
+};
+static thread_local Profiler *g_prof = nullptr;
+
+void prof_begin(const char *name, cudaStream_t s) {
+    if (!g_prof) return;
+    ProfRecord r;
+    r.name = name;
+    cudaEventCreate(&r.a);
+    cudaEventCreate(&r.b);
+    cudaEventRecord(r.a, s);
+    g_prof->recs.push_back(r);
+    g_prof->open = true;
+}
+
+void prof_end(cudaStream_t s) {
+    if (!g_prof || !g_prof->open) return;
+    cudaEventRecord(g_prof->recs.back().b, s);
+    g_prof->open = false;
+}
+
 static ssb_status fail(ssb_status st, const std::string &msg) {
     g_last_error = msg;
     return st;
@@ -339,6 +367,42 @@ ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phas
         SSB_CK(cudaMemcpyAsync(loss_out, c->loss, sizeof(double), cudaMemcpyDeviceToHost, s));
     }
     SSB_CK(cudaStreamSynchronize(s));
+    return SSB_OK;
+}
+
+ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel_time *out,
+                                 int cap, int *n_out, void *cuda_stream) {
+    g_last_error.clear();
+    if (!c || !theta || !n_out || (cap > 0 && !out) || cap < 0) return fail(SSB_ERR_ARG, "bad argument");
+    if (!valid_theta(*theta)) return fail(SSB_ERR_ARG, "non-finite theta");
+    DeviceGuard dg(c->dev);
+    if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    Profiler prof;
+    g_prof = &prof;
+    cudaError_t e = run_objective(c->args(), *theta, c->loss, false, s);
+    g_prof = nullptr;
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    std::vector<ssb_kernel_time> agg;
+    for (auto &r : prof.recs) {
+        float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+        size_t j = 0;
+        while (j < agg.size() && r.name != agg[j].name) ++j;
+        if (j == agg.size()) {
+            ssb_kernel_time t;
+            std::memset(&t, 0, sizeof(t));
+            std::strncpy(t.name, r.name.c_str(), sizeof(t.name) - 1);
+            agg.push_back(t);
+        }
+        agg[j].launches += 1;
+        agg[j].ms += ms;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "profiled objective");
+    *n_out = (int)agg.size();
+    for (int j = 0; j < (int)agg.size() && j < cap; ++j) out[j] = agg[j];
     return SSB_OK;
 }
 

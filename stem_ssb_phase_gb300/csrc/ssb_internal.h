@@ -12,6 +12,11 @@ namespace ssb {
 // Launch-count bookkeeping (every kernel launch of the library goes through this).
 void count_launch(uint64_t n = 1);
 
+// Optional per-launch timing: when a profiling call is active on this thread,
+// prof_begin/prof_end bracket a launch with CUDA events; otherwise they do nothing.
+void prof_begin(const char *name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
 // Per-trial float64 constants derived on the host from theta and the geometry.
 struct TrialHost {
     double cr, sr;        // rotation cos / sin

@@ -189,11 +189,15 @@ static cudaError_t objective_n(const ObjectiveArgs &a, const TrialHost &th, doub
     constexpr int P = N * N;
     cudaError_t e;
     const double inv_nstep = 1.0 / (N * a.step);
+    prof_begin("k_theta_E", s);
     k_theta_E<<<(P + 255) / 256, 256, 0, s>>>(a.E, N, inv_nstep, a.lam, th.cr, th.sr, th.m00,
                                              th.m01, th.m11);
+    prof_end(s);
     count_launch();
+    prof_begin("k_theta_k", s);
     k_theta_k<<<(a.n_bf + 127) / 128, 128, 0, s>>>(a.kturn, a.kalpha, a.n_bf, inv_nstep, th.cr,
                                                   th.sr, th.m00, th.m01, th.m11);
+    prof_end(s);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.S1, 0, sizeof(double) * P, s)) != cudaSuccess) return e;
@@ -219,19 +223,25 @@ static cudaError_t objective_n(const ObjectiveArgs &a, const TrialHost &th, doub
         return e;
     for (int k0 = 0; k0 < a.n_bf; k0 += a.B) {
         const int nb = a.n_bf - k0 < a.B ? a.n_bf - k0 : a.B;
+        prof_begin("k_correct_cols", s);
         k_correct_cols<N><<<dim3((H + CW - 1) / CW, nb), 256, smem1, s>>>(
             a.G, a.X, a.E, a.kgeo, a.kturn, a.tw, tc, k0);
+        prof_end(s);
         count_launch();
+        prof_begin("k_rows_moments", s);
         if (want_object)
             k_rows_moments<N, true><<<N / (1024 / N), 256, smem2, s>>>(a.X, nb, a.S1, a.S2,
                                                                         a.Osum, a.tw);
         else
             k_rows_moments<N, false><<<N / (1024 / N), 256, smem2, s>>>(a.X, nb, a.S1, a.S2,
                                                                          a.Osum, a.tw);
+        prof_end(s);
         count_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    prof_begin("k_loss", s);
     k_loss<<<1, 1024, 0, s>>>(a.S1, a.S2, P, 1.0 / a.n_bf, loss_slot);
+    prof_end(s);
     count_launch();
     return cudaGetLastError();
 }

@@ -164,9 +164,10 @@ def test_single_bf_pixel(ssbgpu, tiny_data):
     ctx = ssbgpu.SSB(g1, counts[40:41])
     th = (30.0, 4.0, 0.3, 0.1)
     ref = oracle.objective(g1, th, counts=counts[40:41])
-    # one BF term: zero variance
+    # one BF term: zero variance; the float32 phi^2 against the float64 S1^2 leaves a
+    # rounding-level residue, bounded relative to the second moment of the phase
     assert ref["loss"] == 0.0
-    assert ctx.loss(th) == 0.0
+    assert abs(ctx.loss(th)) <= 1e-6 * float(np.mean(ref["s2"]))
     mp, _, _ = ctx.reconstruct(th, want_object=False)
     refp = oracle.objective(g1, th, counts=counts[40:41])
     _check_phase(mp.cpu().numpy(), refp)
