@@ -97,6 +97,11 @@ struct ssb_ctx {
     double2 *Osum = nullptr;
     double *loss = nullptr;
     int loss_cap = 0;
+    float2 *Zring = nullptr, *hring = nullptr;
+    double *S2g = nullptr;
+    unsigned *sync = nullptr;
+    int Bk = 0;
+    bool fused = false;
     int *flag = nullptr;
     size_t g_bytes = 0, scratch_bytes = 0;
 
@@ -116,6 +121,11 @@ struct ssb_ctx {
         a.S2 = S2;
         a.Osum = Osum;
         a.loss = loss;
+        a.Zring = Zring;
+        a.hring = hring;
+        a.S2g = S2g;
+        a.sync = sync;
+        a.Bk = Bk;
         a.mode = transfer == SSB_TRANSFER_SSB1 ? 1 : 0;
         a.step = step;
         a.lam = lam;
@@ -127,14 +137,30 @@ struct ssb_ctx {
 
 static void free_ctx(ssb_ctx *c) {
     if (!c) return;
-    void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->X,
-                    c->S1, c->S2, c->Osum, c->loss, c->flag};
+    void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->X, c->S1, c->S2,
+                    c->Osum, c->loss, c->flag, c->Zring, c->hring, c->S2g, c->sync};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete c;
 }
 
 static bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
+
+static cudaError_t evaluate(const ssb_ctx *c, const ssb_params &theta, double *loss_slot,
+                            bool want_object, cudaStream_t s) {
+    return c->fused ? run_objective_fused(c->args(), theta, loss_slot, want_object, s)
+                    : run_objective(c->args(), theta, loss_slot, want_object, s);
+}
+
+// After a fused evaluation: the scheduler's error word (a bounded wait that ran out).
+static ssb_status check_sync(const ssb_ctx *c, cudaStream_t s) {
+    if (!c->fused) return SSB_OK;
+    unsigned h = 0;
+    SSB_CK(cudaMemcpyAsync(&h, c->sync + 1, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+    SSB_CK(cudaStreamSynchronize(s));
+    if (h) return fail(SSB_ERR_TIMEOUT, "a scheduler wait in the fused objective kernel ran out");
+    return SSB_OK;
+}
 
 static bool valid_theta(const ssb_params &t) {
     return std::isfinite(t.C10_nm) && std::isfinite(t.C12_nm) && std::isfinite(t.phi12_rad) &&
@@ -236,9 +262,19 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     SSB_ALLOC(c->kturn, (size_t)c->n_bf, sb);
     SSB_ALLOC(c->E, P, sb);
     SSB_ALLOC(c->tw, (size_t)N, sb);
-    SSB_ALLOC(c->X, (size_t)c->B * P, sb);
+    // SSB2 runs on the persistent fused kernel; SSB1 on the batched two-kernel path
+    c->fused = transfer == SSB_TRANSFER_SSB2;
+    c->Bk = std::min(16, c->n_bf);
+    if (c->fused) {
+        SSB_ALLOC(c->Zring, fused_ring_elems(N, c->Bk), sb);
+        SSB_ALLOC(c->hring, fused_hring_elems(N, c->Bk), sb);
+        SSB_ALLOC(c->S2g, (size_t)fused_row_tasks(N), sb);
+        SSB_ALLOC(c->sync, fused_sync_words(N, c->n_bf, c->Bk), sb);
+    } else {
+        SSB_ALLOC(c->X, (size_t)c->B * P, sb);
+        SSB_ALLOC(c->S2, P, sb);
+    }
     SSB_ALLOC(c->S1, P, sb);
-    SSB_ALLOC(c->S2, P, sb);
     SSB_ALLOC(c->Osum, P, sb);
     c->loss_cap = 4096;
     SSB_ALLOC(c->loss, (size_t)c->loss_cap, sb);
@@ -341,11 +377,13 @@ ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *lo
     for (int t0 = 0; t0 < T; t0 += c->loss_cap) {
         const int tn = std::min(c->loss_cap, T - t0);
         for (int t = 0; t < tn; ++t) {
-            cudaError_t e = run_objective(a, theta[t0 + t], c->loss + t, false, s);
+            cudaError_t e = evaluate(c, theta[t0 + t], c->loss + t, false, s);
             if (e != cudaSuccess) return cuda_fail(e, "objective launch");
         }
         SSB_CK(cudaMemcpyAsync(loss_out + t0, c->loss, sizeof(double) * tn, cudaMemcpyDeviceToHost, s));
         SSB_CK(cudaStreamSynchronize(s));
+        ssb_status st = check_sync(c, s);
+        if (st != SSB_OK) return st;
     }
     return SSB_OK;
 }
@@ -359,7 +397,7 @@ ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phas
     if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
     cudaStream_t s = (cudaStream_t)cuda_stream;
     const ObjectiveArgs a = c->args();
-    cudaError_t e = run_objective(a, *theta, c->loss, object_c64_out != nullptr, s);
+    cudaError_t e = evaluate(c, *theta, c->loss, object_c64_out != nullptr, s);
     if (e != cudaSuccess) return cuda_fail(e, "objective launch");
     if ((e = launch_finalize(a, mean_phase_out, object_c64_out, s)) != cudaSuccess)
         return cuda_fail(e, "finalize launch");
@@ -367,7 +405,7 @@ ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phas
         SSB_CK(cudaMemcpyAsync(loss_out, c->loss, sizeof(double), cudaMemcpyDeviceToHost, s));
     }
     SSB_CK(cudaStreamSynchronize(s));
-    return SSB_OK;
+    return check_sync(c, s);
 }
 
 ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel_time *out,
@@ -380,7 +418,7 @@ ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel
     cudaStream_t s = (cudaStream_t)cuda_stream;
     Profiler prof;
     g_prof = &prof;
-    cudaError_t e = run_objective(c->args(), *theta, c->loss, false, s);
+    cudaError_t e = evaluate(c, *theta, c->loss, false, s);
     g_prof = nullptr;
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     std::vector<ssb_kernel_time> agg;

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/ssb.h"
+#include "ssb_device.cuh"
 
 namespace ssb {
 
@@ -46,9 +47,29 @@ struct ObjectiveArgs {
     double *S1, *S2;        // [N][N] float64 accumulators
     double2 *Osum;          // [N][N] float64 object accumulator (nullable)
     double *loss;           // device float64, one per trial slot
+    // fused (persistent) path
+    float2 *Zring;          // column-pass intermediate ring
+    float2 *hring;          // Nyquist-row Hermitian parts ring
+    double *S2g;            // per row task sums of phi^2
+    unsigned *sync;         // scheduler counters
+    int Bk;                 // BF planes per batch
     int mode;               // 0 SSB2, 1 SSB1
     double step, lam, semi, dalpha;  // geometry (Angstrom, rad)
 };
+
+TrialHost trial_host(const ssb_params &t);
+// float32 per-trial constants for the correction factor
+TrialConst make_trial_const(const ObjectiveArgs &a, const TrialHost &th, int N);
+// per-trial tables E and kturn
+cudaError_t launch_theta_tables(const ObjectiveArgs &a, const TrialHost &th, cudaStream_t s);
+
+// persistent fused path (SSB2): sizes of its buffers and the evaluation itself
+size_t fused_sync_words(int N, int n_bf, int Bk);
+size_t fused_ring_elems(int N, int Bk);
+size_t fused_hring_elems(int N, int Bk);
+int fused_row_tasks(int N);
+cudaError_t run_objective_fused(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,
+                                bool want_object, cudaStream_t s);
 
 // Run one full objective evaluation (S1/S2 zeroed first), loss written to *loss_slot.
 cudaError_t run_objective(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,

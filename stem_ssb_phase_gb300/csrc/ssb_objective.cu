@@ -183,11 +183,31 @@ __global__ void k_finalize(const double *__restrict__ S1, const double2 *__restr
 
 // ---------------------------------------------------------------- host orchestration
 
-template <int N>
-static cudaError_t objective_n(const ObjectiveArgs &a, const TrialHost &th, double *loss_slot,
-                               bool want_object, cudaStream_t s) {
-    constexpr int P = N * N;
-    cudaError_t e;
+TrialHost trial_host(const ssb_params &t) {
+    TrialHost th;
+    th.cr = std::cos(t.rotation_rad);
+    th.sr = std::sin(t.rotation_rad);
+    const double c10 = t.C10_nm * 10.0, c12 = t.C12_nm * 10.0;
+    th.m00 = c10 + c12 * std::cos(2.0 * t.phi12_rad);
+    th.m11 = c10 - c12 * std::cos(2.0 * t.phi12_rad);
+    th.m01 = c12 * std::sin(2.0 * t.phi12_rad);
+    return th;
+}
+
+TrialConst make_trial_const(const ObjectiveArgs &a, const TrialHost &th, int N) {
+    TrialConst tc;
+    tc.cr = (float)th.cr;
+    tc.sr = (float)th.sr;
+    tc.lam = (float)a.lam;
+    tc.inv_nstep = (float)(1.0 / (N * a.step));
+    tc.semi = (float)a.semi;
+    tc.inv_dalpha = (float)(1.0 / a.dalpha);
+    tc.mode = a.mode;
+    return tc;
+}
+
+cudaError_t launch_theta_tables(const ObjectiveArgs &a, const TrialHost &th, cudaStream_t s) {
+    const int N = a.N, P = N * N;
     const double inv_nstep = 1.0 / (N * a.step);
     prof_begin("k_theta_E", s);
     k_theta_E<<<(P + 255) / 256, 256, 0, s>>>(a.E, N, inv_nstep, a.lam, th.cr, th.sr, th.m00,
@@ -199,21 +219,20 @@ static cudaError_t objective_n(const ObjectiveArgs &a, const TrialHost &th, doub
                                                   th.sr, th.m00, th.m01, th.m11);
     prof_end(s);
     count_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int N>
+static cudaError_t objective_n(const ObjectiveArgs &a, const TrialHost &th, double *loss_slot,
+                               bool want_object, cudaStream_t s) {
+    constexpr int P = N * N;
+    cudaError_t e;
+    if ((e = launch_theta_tables(a, th, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.S1, 0, sizeof(double) * P, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.S2, 0, sizeof(double) * P, s)) != cudaSuccess) return e;
     if (want_object && (e = cudaMemsetAsync(a.Osum, 0, sizeof(double2) * P, s)) != cudaSuccess)
         return e;
-
-    TrialConst tc;
-    tc.cr = (float)th.cr;
-    tc.sr = (float)th.sr;
-    tc.lam = (float)a.lam;
-    tc.inv_nstep = (float)inv_nstep;
-    tc.semi = (float)a.semi;
-    tc.inv_dalpha = (float)(1.0 / a.dalpha);
-    tc.mode = a.mode;
-
+    const TrialConst tc = make_trial_const(a, th, N);
     constexpr int CW = kColsPerBlock;
     constexpr int H = N / 2 + 1;
     const size_t smem1 = (size_t)(N + 4 * CW * N) * sizeof(float2);
@@ -244,17 +263,6 @@ static cudaError_t objective_n(const ObjectiveArgs &a, const TrialHost &th, doub
     prof_end(s);
     count_launch();
     return cudaGetLastError();
-}
-
-static TrialHost trial_host(const ssb_params &t) {
-    TrialHost th;
-    th.cr = std::cos(t.rotation_rad);
-    th.sr = std::sin(t.rotation_rad);
-    const double c10 = t.C10_nm * 10.0, c12 = t.C12_nm * 10.0;
-    th.m00 = c10 + c12 * std::cos(2.0 * t.phi12_rad);
-    th.m11 = c10 - c12 * std::cos(2.0 * t.phi12_rad);
-    th.m01 = c12 * std::sin(2.0 * t.phi12_rad);
-    return th;
 }
 
 cudaError_t run_objective(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,

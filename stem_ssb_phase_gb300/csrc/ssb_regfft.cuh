@@ -1,0 +1,130 @@
+// Register-resident FFT of length N by a group of T = N/8 threads, each holding 8 points.
+//
+// Thread j of the group holds x[j + T r] (r = 0..7) on entry and X[j + T r] on exit
+// (natural order both sides).  Passes follow Stockham's self-sorting schedule (radix 8,
+// then a final radix 4 or 2 when log2 N is not a multiple of 3); between passes the
+// points go through a padded shared-memory buffer of N + N/8 complex values per group.
+// With T threads, a radix-R pass has N/R butterflies: butterfly b reads x[b + (N/R) q],
+// twists it by exp(S 2 pi i q (b mod Ns) / (Ns R)), takes the R-point DFT and writes
+// y[(b - b mod Ns) R + b mod Ns + Ns q].  Because thread j's registers hold exactly the
+// inputs of butterflies j + T m, no shuffle is needed, and the last pass leaves its
+// outputs in registers in natural order.
+#pragma once
+
+#include "ssb_device.cuh"
+
+namespace ssb {
+
+// Padded shared-memory index: one spare slot every 8 complex values keeps the pass
+// exchanges free of bank conflicts for 64-bit accesses.
+__device__ __forceinline__ int padx(int i) { return i + (i >> 3); }
+
+template <int N>
+struct RegFFT {
+    static constexpr int T = N / 8;
+    static constexpr int SMEM = N + N / 8;  // complex values per group
+    static constexpr int LOG2N = N == 32 ? 5 : N == 64 ? 6 : N == 128 ? 7 : N == 256 ? 8 : 9;
+    static constexpr int N8 = LOG2N / 3;       // radix-8 passes
+    static constexpr int TAIL = LOG2N - 3 * N8; // 0, 1 (radix 2) or 2 (radix 4)
+};
+
+// 8-point DFT in registers with exponent sign S, by one radix-2 split into two 4-point DFTs.
+template <int S>
+__device__ __forceinline__ void dft8(float2 (&v)[8]) {
+    constexpr float R2 = 0.70710678118654752f;
+    float2 a[4], b[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        a[q] = cadd(v[q], v[q + 4]);
+        b[q] = csub(v[q], v[q + 4]);
+    }
+    // b_q *= exp(S 2 pi i q / 8)
+    b[1] = make_float2(R2 * (b[1].x - S * b[1].y), R2 * (b[1].y + S * b[1].x));
+    b[2] = S > 0 ? make_float2(-b[2].y, b[2].x) : make_float2(b[2].y, -b[2].x);
+    b[3] = make_float2(R2 * (-b[3].x - S * b[3].y), R2 * (-b[3].y + S * b[3].x));
+    dft4<S>(a[0], a[1], a[2], a[3]);
+    dft4<S>(b[0], b[1], b[2], b[3]);
+    v[0] = a[0]; v[1] = b[0]; v[2] = a[1]; v[3] = b[1];
+    v[4] = a[2]; v[5] = b[2]; v[6] = a[3]; v[7] = b[3];
+}
+
+// One Stockham pass of radix R (8, 4 or 2) over the group's registers, span Ns.
+// If LAST, results stay in registers (natural order); otherwise they are written to sm
+// and read back in the next pass's input order.  bar() synchronises the group.
+template <int N, int R, int S, bool LAST, typename Bar>
+__device__ __forceinline__ void stockham_pass(float2 (&v)[8], float2 *sm, const float2 *tw,
+                                              int j, int Ns, Bar bar) {
+    constexpr int T = N / 8;
+    constexpr int NB = N / R;        // butterflies
+    constexpr int PER = NB / T;      // butterflies per thread (1, 2 or 4)
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+        const int b = j + T * m;
+        const int k = b & (Ns - 1);
+        float2 u[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) u[q] = v[m + PER * q];
+        if (Ns > 1) {
+            const int step = N / (Ns * R);
+#pragma unroll
+            for (int q = 1; q < R; ++q) u[q] = cmul(u[q], twid<S>(tw, q * k * step));
+        }
+        if (R == 8) {
+            float2 w[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w[q] = u[q];
+            dft8<S>(w);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) u[q] = w[q];
+        } else if (R == 4) {
+            dft4<S>(u[0], u[1], u[2], u[3]);
+        } else {
+            const float2 t = u[1];
+            u[1] = csub(u[0], t);
+            u[0] = cadd(u[0], t);
+        }
+        if (LAST) {
+            // final pass: Ns = N/R, output index b + Ns q = j + T (m + PER q)
+#pragma unroll
+            for (int q = 0; q < R; ++q) v[m + PER * q] = u[q];
+        } else {
+            const int o = (b - k) * R + k;
+#pragma unroll
+            for (int q = 0; q < R; ++q) sm[padx(o + Ns * q)] = u[q];
+        }
+    }
+    if (!LAST) {
+        bar();
+#pragma unroll
+        for (int r = 0; r < 8; ++r) v[r] = sm[padx(j + T * r)];
+        bar();
+    }
+}
+
+// Full transform.  sm: this group's N + N/8 complex scratch; tw: exp(+2 pi i m/N), m < N.
+template <int N, int S, typename Bar>
+__device__ __forceinline__ void reg_fft(float2 (&v)[8], float2 *sm, const float2 *tw, int j,
+                                        Bar bar) {
+    using F = RegFFT<N>;
+    int Ns = 1;
+    if (F::TAIL == 0) {
+#pragma unroll
+        for (int p = 0; p < F::N8 - 1; ++p) {
+            stockham_pass<N, 8, S, false>(v, sm, tw, j, Ns, bar);
+            Ns *= 8;
+        }
+        stockham_pass<N, 8, S, true>(v, sm, tw, j, Ns, bar);
+    } else {
+#pragma unroll
+        for (int p = 0; p < F::N8; ++p) {
+            stockham_pass<N, 8, S, false>(v, sm, tw, j, Ns, bar);
+            Ns *= 8;
+        }
+        if (F::TAIL == 2)
+            stockham_pass<N, 4, S, true>(v, sm, tw, j, Ns, bar);
+        else
+            stockham_pass<N, 2, S, true>(v, sm, tw, j, Ns, bar);
+    }
+}
+
+}  // namespace ssb

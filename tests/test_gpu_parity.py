@@ -175,12 +175,23 @@ def test_single_bf_pixel(ssbgpu, tiny_data):
 
 def test_inactive_bf_pixels_give_zero_phase(ssbgpu, tiny_data):
     w, geom, counts, _ = tiny_data
-    g2 = ssb_synth.make_geometry(w)
-    g2.semiangle_mrad = 1.0  # every BF pixel outside the probe aperture
-    ctx = ssbgpu.SSB(g2, counts)
-    assert ctx.loss((50.0, 3.0, 0.2, 0.1)) == 0.0
-    mp, _, _ = ctx.reconstruct((50.0, 3.0, 0.2, 0.1), want_object=False)
+    # BF pixels at least 2 px off axis with a 1 mrad probe aperture: a(alpha_k) = 0
+    r = np.hypot(geom.bf_det_yx[:, 0], geom.bf_det_yx[:, 1])
+    sub = np.nonzero(r >= 2.0)[0]
+    g2 = ssb_synth.make_geometry(w, bf_subset=sub)
+    g2.semiangle_mrad = 1.0
+    ctx = ssbgpu.SSB(g2, counts[sub])
+    th = (50.0, 3.0, 0.2, 0.1)
+    assert oracle.objective(g2, th, counts=counts[sub])["loss"] == 0.0
+    assert ctx.loss(th) == 0.0
+    mp, _, _ = ctx.reconstruct(th, want_object=False)
     assert float(mp.abs().max()) == 0.0
+    # mixed: the inactive pixels stay in the normalisation
+    g3 = ssb_synth.make_geometry(w)
+    g3.semiangle_mrad = 4.0
+    ctx3 = ssbgpu.SSB(g3, counts)
+    ref = oracle.objective(g3, th, counts=counts)
+    assert abs(ctx3.loss(th) - ref["loss"]) <= LOSS_RTOL * ref["loss"]
 
 
 @pytest.mark.parametrize("scan_n,det_n,radius,n_sub", [(64, 32, 8.0, None), (512, 192, 53.3, 24),
