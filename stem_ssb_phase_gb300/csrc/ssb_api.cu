@@ -11,6 +11,13 @@
 #include "ssb_device.cuh"
 #include "ssb_internal.h"
 
+#ifndef SSB_FUSED_BK
+#define SSB_FUSED_BK 16
+#endif
+#ifndef SSB_FUSED_RING
+#define SSB_FUSED_RING 4
+#endif
+
 namespace ssb {
 
 static std::atomic<uint64_t> g_launches{0};
@@ -100,7 +107,7 @@ struct ssb_ctx {
     float2 *Zring = nullptr, *hring = nullptr;
     double *S2g = nullptr;
     unsigned *sync = nullptr;
-    int Bk = 0;
+    int Bk = 0, D = 0;
     bool fused = false;
     int *flag = nullptr;
     size_t g_bytes = 0, scratch_bytes = 0;
@@ -126,6 +133,7 @@ struct ssb_ctx {
         a.S2g = S2g;
         a.sync = sync;
         a.Bk = Bk;
+        a.D = D;
         a.mode = transfer == SSB_TRANSFER_SSB1 ? 1 : 0;
         a.step = step;
         a.lam = lam;
@@ -264,10 +272,14 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     SSB_ALLOC(c->tw, (size_t)N, sb);
     // SSB2 runs on the persistent fused kernel; SSB1 on the batched two-kernel path
     c->fused = transfer == SSB_TRANSFER_SSB2;
-    c->Bk = std::min(16, c->n_bf);
+    // batch size and ring depth of the fused path: several short batches in flight keep
+    // the column work flowing while slow row tasks drain the oldest slots, within an
+    // L2-sized ring (about 50 MB at N = 512)
+    c->Bk = std::min(SSB_FUSED_BK, c->n_bf);
+    c->D = SSB_FUSED_RING;
     if (c->fused) {
-        SSB_ALLOC(c->Zring, fused_ring_elems(N, c->Bk), sb);
-        SSB_ALLOC(c->hring, fused_hring_elems(N, c->Bk), sb);
+        SSB_ALLOC(c->Zring, fused_ring_elems(N, c->Bk, c->D), sb);
+        SSB_ALLOC(c->hring, fused_hring_elems(N, c->Bk, c->D), sb);
         SSB_ALLOC(c->S2g, (size_t)fused_row_tasks(N), sb);
         SSB_ALLOC(c->sync, fused_sync_words(N, c->n_bf, c->Bk), sb);
     } else {

@@ -101,6 +101,10 @@ struct TrialConst {
     float semi;         // aperture semiangle (rad)
     float inv_dalpha;   // 1 / detector sampling (1/rad)
     int mode;           // 0 = SSB2, 1 = SSB1
+    // lambda Q' = (lxs sx + lxy sy, lys sx + lyy sy) for signed bins (sx, sy)
+    float lxs, lxy, lys, lyy;
+    float inner2;       // |alpha|^2 at or below which a(alpha) = 1 (negative: never)
+    float outer2;       // |alpha|^2 at or above which a(alpha) = 0
 };
 
 // Amplitudes below this are exactly zero transfer: a scan grid commensurate with the
@@ -112,6 +116,60 @@ __device__ __forceinline__ float soft_aperture(float ax, float ay, float semi, f
     const float r = sqrtf(fmaf(ax, ax, ay * ay));
     const float a = fminf(fmaxf(fmaf(semi - r, inv_da, 0.5f), 0.0f), 1.0f);
     return a < kApertureFloor ? 0.0f : a;
+}
+
+// Soft aperture from |alpha|^2 with exact inside/outside shortcuts: a = 1 for
+// |alpha| <= alpha_c - d_alpha/2 and a = 0 for |alpha| >= alpha_c + d_alpha/2 need no
+// square root; the rim between them takes the full expression and the zero floor.
+__device__ __forceinline__ float aperture_r2(float r2, const TrialConst &tc) {
+    if (r2 >= tc.outer2) return 0.0f;
+    if (r2 <= tc.inner2) return 1.0f;
+    const float r = r2 > 0.0f ? r2 * rsqrtf(r2) : 0.0f;
+    const float a = fminf(fmaxf(fmaf(tc.semi - r, tc.inv_dalpha, 0.5f), 0.0f), 1.0f);
+    return a < kApertureFloor ? 0.0f : a;
+}
+
+// SSB2 correction of one G value at signed bins (sx, sy), with the per-column terms
+// hoisted by the caller: lx0 = lxs sx, ly0 = lys sx, phx = b_x sx (turn fraction).
+// Same algebra as correction_factor below; DC and a_k = 0 are handled by the caller.
+__device__ __forceinline__ float2 correct_ssb2(float2 g, int sy, float2 e, float gx, float gy,
+                                               uint32_t phx, uint32_t by, float lx0, float ly0,
+                                               const TrialConst &tc) {
+    const float fsy = (float)sy;
+    const float lx = fmaf(tc.lxy, fsy, lx0), ly = fmaf(tc.lyy, fsy, ly0);
+    const float dmx = gx - lx, dmy = gy - ly, dpx = gx + lx, dpy = gy + ly;
+    const float am = aperture_r2(fmaf(dmx, dmx, dmy * dmy), tc);
+    const float ap = aperture_r2(fmaf(dpx, dpx, dpy * dpy), tc);
+    const float dx = (am - ap) * e.x, dy = (am + ap) * e.y;
+    const float d2 = fmaf(dx, dx, dy * dy);
+    if (!(d2 > 0.0f)) return make_float2(0.0f, 0.0f);  // zero transfer
+    const uint32_t ph = phx + by * (uint32_t)sy;
+    float sb, cb;
+    __sincosf((float)(int32_t)ph * 1.4629180792671596e-09f, &sb, &cb);  // 2 pi ph / 2^32
+    const float inv = rsqrtf(d2);
+    return cmul(g, cmul(make_float2(dx * inv, -dy * inv), make_float2(cb, sb)));
+}
+
+// Phase atan2(y, x) in (-pi, pi]: octant reduction to a = min/max in [0, 1], an odd
+// degree-15 polynomial in a fitted to atan on [0, 1] for this library (float32 Horner
+// error below 1.4e-7 rad), then the unfolding pi/2 - p, pi - p and the sign of y.
+__device__ __forceinline__ float fast_atan2(float y, float x) {
+    const float ax = fabsf(x), ay = fabsf(y);
+    const float mx = fmaxf(ax, ay), mn = fminf(ax, ay);
+    const float a = mx > 0.0f ? __fdividef(mn, mx) : 0.0f;
+    const float s = a * a;
+    float p = -4.054552875e-03f;
+    p = fmaf(p, s, 2.186291292e-02f);
+    p = fmaf(p, s, -5.591227114e-02f);
+    p = fmaf(p, s, 9.642194211e-02f);
+    p = fmaf(p, s, -1.390862912e-01f);
+    p = fmaf(p, s, 1.994656622e-01f);
+    p = fmaf(p, s, -3.332985938e-01f);
+    p = fmaf(p, s, 9.999993443e-01f);
+    float r = p * a;
+    if (ay > ax) r = 1.57079632679489662f - r;
+    if (x < 0.0f) r = 3.14159265358979324f - r;
+    return copysignf(r, y);
 }
 
 // Correction factor F_k(Q) such that C_k(Q) = G_k(Q) F_k(Q).

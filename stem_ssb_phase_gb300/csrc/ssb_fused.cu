@@ -34,7 +34,7 @@
 namespace ssb {
 
 constexpr int kFusedThreads = 256;
-constexpr int kRingSlots = 3;
+constexpr int kPts = 16;                    // points per thread in every transform
 constexpr unsigned kWaitLimit = 1u << 24;  // polls of ~0.1-1 us each before giving up
 
 struct FusedParams {
@@ -43,32 +43,37 @@ struct FusedParams {
     const float4 *kgeo;   // per BF (alpha_x, alpha_y, a_k, 0)
     const uint2 *kturn;   // per BF bilinear phase slopes
     const float2 *tw;     // [N] exp(+2 pi i m/N)
-    float2 *Z;            // ring [D][Bk][N/4][H][4]
-    float2 *hrow;         // ring [D][Bk][H]
+    float2 *Z;            // ring [D][Bk][N][LDZ], rows of the column-pass output
+    float2 *hrow;         // ring [D][Bk][LDZ], Nyquist-row Hermitian parts
     double *S1;           // [P]
     double *S2g;          // [row tasks]
     double2 *Osum;        // [P] (object redraw only)
-    unsigned *sync;       // ticket, error, col_done[nbatch], row_done[nbatch], chain[row tasks]
+    unsigned *sync;       // ticket, error, col_done[nbatch], plane_free[nbatch][Bk], chain[row tasks]
     int n_bf, Bk, nbatch;
+    int D;                // ring slots (batches in flight)
     TrialConst tc;
 };
 
 template <int N>
 struct FusedShape {
-    static constexpr int T = N / 8;                 // threads per transform
+    static constexpr int T = N / kPts;              // threads per transform
+    static constexpr int GROUPS = kFusedThreads / T;  // transforms per block
     static constexpr int H = N / 2 + 1;             // half-plane columns
-    static constexpr int CW = kFusedThreads / T;    // columns per column task
-    static constexpr int RT = CW < N ? CW : N;      // rows per row task (multiple of 4)
+    static constexpr int CW = GROUPS;               // columns per column task
+    static constexpr int RT = GROUPS < N ? GROUPS : N;  // rows per row task (multiple of 4)
     static constexpr int CT = (H + CW - 1) / CW;    // column tasks per plane
     static constexpr int NR = N / RT;               // row tasks per trial
-    static constexpr int SMF = RegFFT<N>::SMEM;     // FFT scratch per group
+    static constexpr int SMF = RegFFT<N, kPts>::SMEM;  // FFT scratch per group
+    static constexpr int LDZ = (H + 7) / 8 * 8;     // intermediate row stride (64 B multiple)
+    static constexpr int CHUNKS = LDZ / 2;          // 16-byte chunks per row
+    static constexpr int LDS = CW + 1;              // column-task staging stride
     // dynamic shared memory layout, in float2 units
-    static constexpr int OFF_TW = 0;
-    static constexpr int OFF_FFT = OFF_TW + N;
-    static constexpr int OFF_TILE = OFF_FFT + CW * SMF;
-    static constexpr int OFF_H = OFF_TILE + RT * H;
-    static constexpr int OFF_RED = OFF_H + ((H + 1) & ~1);
-    static constexpr int TOTAL = OFF_RED + kFusedThreads;  // reduction uses 8 bytes each
+    static constexpr int OFF_TW = 0;                                // padded twiddles
+    static constexpr int OFF_FFT = OFF_TW + (N + N / 8 + 2 + 1) / 2 * 2;
+    static constexpr int OFF_TILE = OFF_FFT + GROUPS * SMF;         // [2][RT + 1][LDZ]
+    static constexpr int TILEBUF = (RT + 1) * LDZ;                  // rows, then h
+    static constexpr int OFF_RED = OFF_TILE + 2 * TILEBUF;
+    static constexpr int TOTAL = OFF_RED + 16;  // 8 warp partials (8 bytes each)
     static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float2);
 };
 
@@ -77,6 +82,14 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int K>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory"); }
 
 __device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -97,7 +110,8 @@ __device__ bool wait_at_least(const unsigned *addr, unsigned target, unsigned *e
     return true;
 }
 
-__device__ __forceinline__ void block_bar() { __syncthreads(); }
+// Transforms never span warps (T <= 32), so their exchanges need only warp sync.
+__device__ __forceinline__ void warp_bar() { __syncwarp(); }
 
 // ---------------------------------------------------------------- column task
 
@@ -107,120 +121,174 @@ __device__ void column_task(const FusedParams &p, float2 *smem, int b, int idx) 
     const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
     const int kk = idx / S::CT, ct = idx - kk * S::CT;
     const int k = b * p.Bk + kk;
-    const int slot = b % kRingSlots;
+    const int slot = b % p.D;
     const int nx = ct * S::CW + grp;
     const bool valid = nx < S::H;
-    const float4 geo = p.kgeo[k];
-    const uint2 bt = p.kturn[k];
-    float2 v[8];
+    const float4 geo = __ldg(p.kgeo + k);
+    const uint2 bt = __ldg(p.kturn + k);
+    float2 v[kPts];
     if (valid) {
-        const float2 *g = p.G + ((size_t)k * S::H + nx) * N;
-        const float2 *e = p.Et + (size_t)nx * N;
+        const float2 *g = p.G + ((size_t)k * S::H + nx) * N + j;
+        const float2 *e = p.Et + (size_t)nx * N + j;
+        float2 ev[kPts];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < kPts; ++r) {
+            v[r] = __ldcs(g + S::T * r);
+            ev[r] = __ldg(e + S::T * r);
+        }
+        const int sx = nx < N / 2 ? nx : nx - N;
+        const float lx0 = p.tc.lxs * (float)sx, ly0 = p.tc.lys * (float)sx;
+        const uint32_t phx = bt.x * (uint32_t)sx;
+        const bool active = geo.z > 0.0f;  // a(alpha_k) = 0: only the DC term survives
+#pragma unroll
+        for (int r = 0; r < kPts; ++r) {
             const int ny = j + S::T * r;
-            const float2 gv = __ldcs(g + ny);
-            v[r] = cmul(gv, correction_factor<N>(ny, nx, geo, bt, __ldg(e + ny), p.tc));
-            if (r == 4 && j == 0 && nx >= 1 && nx < N / 2) {
-                // Nyquist row: its mirror bin carries its own correction (no partner)
-                const float2 f2 = correction_factor<N>(N / 2, N - nx, geo, bt,
-                                                       __ldg(p.Et + (size_t)(N - nx) * N + N / 2), p.tc);
-                const float2 c2 = cmul(cconj(gv), f2);
-                const float2 h = make_float2(0.5f * (v[r].x + c2.x), 0.5f * (v[r].y - c2.y));
-                __stcg(p.hrow + ((size_t)slot * p.Bk + kk) * S::H + nx, h);
+            const int sy = ny < N / 2 ? ny : ny - N;
+            const float2 gv = v[r];
+            float2 c = active ? correct_ssb2(gv, sy, ev[r], geo.x, geo.y, phx, bt.y, lx0, ly0, p.tc)
+                              : make_float2(0.f, 0.f);
+            if ((nx | ny) == 0) c = gv;  // C(0) = G(0)
+            if (r == kPts / 2 && j == 0 && nx >= 1 && nx < N / 2) {
+                // Nyquist row (ny = N/2): the mirror bin N - nx has no partner and carries
+                // its own correction, at signed bins (-nx, -N/2)
+                const float2 em = __ldg(p.Et + (size_t)(N - nx) * N + N / 2);
+                const float2 c2 = active ? correct_ssb2(cconj(gv), -N / 2, em, geo.x, geo.y,
+                                                        0u - phx, bt.y, -lx0, -ly0, p.tc)
+                                         : make_float2(0.f, 0.f);
+                const float2 h = make_float2(0.5f * (c.x + c2.x), 0.5f * (c.y - c2.y));
+                __stcg(p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ + nx, h);
             }
+            v[r] = c;
         }
     } else {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) v[r] = make_float2(0.f, 0.f);
+        for (int r = 0; r < kPts; ++r) v[r] = make_float2(0.f, 0.f);
     }
-    reg_fft<N, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, block_bar);
-    if (valid) {
-        float2 *z = p.Z + ((size_t)slot * p.Bk + kk) * (size_t)(N / 4) * S::H * 4;
+    reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
+    // transpose the task's CW columns through shared memory (aliasing the FFT scratch)
+    // so that each output row segment of CW values is written as whole sectors
+    __syncthreads();
+    float2 *stage = smem + S::OFF_FFT;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int ry = j + S::T * r;
-            __stcg(z + ((size_t)(ry >> 2) * S::H + nx) * 4 + (ry & 3), v[r]);
-        }
+    for (int r = 0; r < kPts; ++r) stage[(j + S::T * r) * S::LDS + grp] = v[r];
+    __syncthreads();
+    const int c0 = ct * S::CW;
+    const int ncol = S::H - c0 < S::CW ? S::H - c0 : S::CW;
+    float2 *z = p.Z + ((size_t)slot * p.Bk + kk) * (size_t)N * S::LDZ + c0;
+    for (int e = tid; e < N * S::CW; e += kFusedThreads) {
+        const int ry = e / S::CW, c = e - ry * S::CW;
+        if (c < ncol) __stcg(z + (size_t)ry * S::LDZ + c, stage[ry * S::LDS + c]);
     }
 }
 
 // ---------------------------------------------------------------- row task
 
+// Start the asynchronous copy of one plane's RT rows and its Nyquist terms into buf.
+template <int N>
+__device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk, int ry0,
+                                          float2 *buf) {
+    using S = FusedShape<N>;
+    const float2 *zsrc = p.Z + (((size_t)slot * p.Bk + kk) * N + ry0) * S::LDZ;
+    for (int e = threadIdx.x; e < S::RT * S::CHUNKS; e += kFusedThreads)
+        cp_async16(buf + 2 * e, zsrc + 2 * e);
+    const float2 *hsrc = p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ;
+    for (int e = threadIdx.x; e < S::CHUNKS; e += kFusedThreads)
+        cp_async16(buf + S::RT * S::LDZ + 2 * e, hsrc + 2 * e);
+    cp_async_commit();
+}
+
 template <int N, bool OBJ>
-__device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int planes) {
+__device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int planes,
+                         unsigned *plane_free, unsigned *chain, unsigned *err, int *s_ok) {
     using S = FusedShape<N>;
     const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
-    const int slot = b % kRingSlots;
+    const int slot = b % p.D;
     const int ry0 = rt * S::RT;
     const bool active = grp < S::RT;                // N = 32 leaves some groups idle
-    const int ry = ry0 + (active ? grp : 0);        // this group's row
-    const int lt = grp >> 2, lb = grp & 3;          // tile within the task, row within tile
+    const int lr = active ? grp : 0;
+    const int ry = ry0 + lr;
     const float sgn2 = (ry & 1) ? -2.0f : 2.0f;     // 2 (-1)^ry
-    float2 *tile = smem + S::OFF_TILE;
-    float2 *hs = smem + S::OFF_H;
-    float acc1[8];
-    float2 acco[8];
+    float2 *tiles = smem + S::OFF_TILE;
+    float acc1[kPts];
+    float2 acco[kPts];
     float acc2 = 0.f;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < kPts; ++r) {
         acc1[r] = 0.f;
         acco[r] = make_float2(0.f, 0.f);
     }
+    row_issue<N>(p, slot, 0, ry0, tiles);
     for (int kk = 0; kk < planes; ++kk) {
-        // stage this task's RT/4 row tiles (contiguous) and the plane's Nyquist terms
-        const float4 *zsrc = reinterpret_cast<const float4 *>(
-            p.Z + (((size_t)slot * p.Bk + kk) * (size_t)(N / 4) + ry0 / 4) * S::H * 4);
-        float4 *tdst = reinterpret_cast<float4 *>(tile);
-        for (int i = tid; i < S::RT * S::H / 2; i += kFusedThreads) tdst[i] = __ldcg(zsrc + i);
-        const float2 *hsrc = p.hrow + ((size_t)slot * p.Bk + kk) * S::H;
-        for (int i = tid; i < S::H; i += kFusedThreads) hs[i] = __ldcg(hsrc + i);
-        __syncthreads();
-        float2 v[8];
+        float2 *cur = tiles + (kk & 1) * S::TILEBUF;
+        __syncthreads();  // everyone is done with the other buffer (plane kk - 1)
+        if (kk + 1 < planes) {
+            row_issue<N>(p, slot, kk + 1, ry0, tiles + ((kk + 1) & 1) * S::TILEBUF);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();  // plane kk has landed for every thread
+        if (tid == 0) {
+            // this task no longer needs plane kk of the slot: columns of batch b + D may
+            // overwrite it once every row task has passed it
+            __threadfence();
+            atomicAdd(plane_free + (size_t)b * p.Bk + kk, 1u);
+        }
+        const float2 *row = cur + lr * S::LDZ;
+        const float2 *hs = cur + S::RT * S::LDZ;
+        float2 v[kPts];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < kPts; ++r) {
             const int nx = j + S::T * r;
             if (!active) {
                 v[r] = make_float2(0.f, 0.f);
             } else if (nx <= N / 2) {
-                v[r] = tile[((size_t)lt * S::H + nx) * 4 + lb];
+                v[r] = row[nx];
             } else {
                 const int m = N - nx;
-                const float2 z = tile[((size_t)lt * S::H + m) * 4 + lb];
+                const float2 z = row[m];
                 const float2 h = hs[m];
                 v[r] = make_float2(fmaf(sgn2, h.x, -z.x), fmaf(-sgn2, h.y, z.y));
             }
         }
-        reg_fft<N, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, block_bar);
+        reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const float phi = atan2f(v[r].y, v[r].x);
+        for (int r = 0; r < kPts; ++r) {
+            const float phi = fast_atan2(v[r].y, v[r].x);
             acc1[r] += phi;
             acc2 = fmaf(phi, phi, acc2);
             if (OBJ) acco[r] = cadd(acco[r], v[r]);
         }
-        __syncthreads();  // tile and hs are reloaded for the next plane
     }
-    // add this batch into the float64 accumulators (batches arrive in order per task)
+    // Add this batch into the float64 accumulators.  Only this update is ordered: it
+    // waits until the previous batch's task for the same rows has made its own update,
+    // which keeps the per-pixel summation order fixed while the tasks themselves overlap.
+    if (tid == 0) *s_ok = wait_at_least(chain + rt, (unsigned)b, err);
+    __syncthreads();
+    if (active && *s_ok) {
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        if (!active) break;
-        const size_t i = (size_t)ry * N + j + S::T * r;
-        p.S1[i] = __ldcg(p.S1 + i) + (double)acc1[r];
-        if (OBJ) {
-            const double2 o = __ldcg(p.Osum + i);
-            p.Osum[i] = make_double2(o.x + acco[r].x, o.y + acco[r].y);
+        for (int r = 0; r < kPts; ++r) {
+            const size_t i = (size_t)ry * N + j + S::T * r;
+            p.S1[i] = __ldcg(p.S1 + i) + (double)acc1[r];
+            if (OBJ) {
+                const double2 o = __ldcg(p.Osum + i);
+                p.Osum[i] = make_double2(o.x + acco[r].x, o.y + acco[r].y);
+            }
         }
     }
-    double *red = reinterpret_cast<double *>(smem + S::OFF_RED);
-    red[tid] = active ? (double)acc2 : 0.0;
-    __syncthreads();
+    // sum of phi^2: warp shuffles, then the 8 warp partials in a fixed order
+    double w2 = active ? (double)acc2 : 0.0;
 #pragma unroll
-    for (int s = kFusedThreads / 2; s > 0; s >>= 1) {
-        if (tid < s) red[tid] += red[tid + s];
-        __syncthreads();
+    for (int o = 16; o > 0; o >>= 1) w2 += __shfl_down_sync(0xffffffffu, w2, o);
+    double *red = reinterpret_cast<double *>(smem + S::OFF_RED);
+    if ((tid & 31) == 0) red[tid >> 5] = w2;
+    __syncthreads();
+    if (tid == 0) {
+        double t = 0.0;
+#pragma unroll
+        for (int w = 0; w < kFusedThreads / 32; ++w) t += red[w];
+        if (*s_ok) p.S2g[rt] = __ldcg(p.S2g + rt) + t;
     }
-    if (tid == 0) p.S2g[rt] = __ldcg(p.S2g + rt) + red[0];
 }
 
 // ---------------------------------------------------------------- scheduler
@@ -230,7 +298,6 @@ struct Task {
     int b, idx;
 };
 
-template <int N>
 __device__ __forceinline__ int planes_in(const FusedParams &p, int b) {
     return b < p.nbatch - 1 ? p.Bk : p.n_bf - p.Bk * (p.nbatch - 1);
 }
@@ -241,9 +308,8 @@ template <int N>
 __device__ Task decode_ticket(const FusedParams &p, unsigned t) {
     using S = FusedShape<N>;
     const unsigned nc_full = (unsigned)p.Bk * S::CT;
-    const unsigned nc_last = (unsigned)planes_in<N>(p, p.nbatch - 1) * S::CT;
+    const unsigned nc_last = (unsigned)planes_in(p, p.nbatch - 1) * S::CT;
     const unsigned nr = S::NR;
-    Task task{2, 0, 0};
     const unsigned nc0 = p.nbatch == 1 ? nc_last : nc_full;
     if (t < nc0) return Task{0, 0, (int)t};
     t -= nc0;
@@ -262,22 +328,22 @@ __device__ Task decode_ticket(const FusedParams &p, unsigned t) {
         t -= nr;
     }
     if (t < nr) return Task{1, p.nbatch - 1, (int)t};
-    return task;
+    return Task{2, 0, 0};
 }
 
 template <int N, bool OBJ>
-__global__ void __launch_bounds__(kFusedThreads) k_fused(FusedParams p) {
+__global__ void __launch_bounds__(kFusedThreads, 2) k_fused(FusedParams p) {
     using S = FusedShape<N>;
-    extern __shared__ float2 smem[];
+    extern __shared__ __align__(16) float2 smem[];
     __shared__ unsigned s_ticket;
     __shared__ int s_ok;
     const int tid = threadIdx.x;
-    for (int i = tid; i < N; i += kFusedThreads) smem[S::OFF_TW + i] = p.tw[i];
+    for (int i = tid; i < N; i += kFusedThreads) smem[S::OFF_TW + padx(i)] = p.tw[i];
     unsigned *ticket = p.sync;
     unsigned *err = p.sync + 1;
     unsigned *col_done = p.sync + 2;
-    unsigned *row_done = col_done + p.nbatch;
-    unsigned *chain = row_done + p.nbatch;
+    unsigned *plane_free = col_done + p.nbatch;
+    unsigned *chain = plane_free + (size_t)p.nbatch * p.Bk;
     __syncthreads();
     while (true) {
         if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
@@ -287,11 +353,11 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused(FusedParams p) {
         if (tid == 0) {
             bool ok = true;
             if (task.kind == 0) {
-                if (task.b >= kRingSlots)  // ring slot still being read by rows of b - D
-                    ok = wait_at_least(row_done + task.b - kRingSlots, (unsigned)S::NR, err);
+                if (task.b >= p.D)  // this plane of the ring slot is read by rows of b - D
+                    ok = wait_at_least(plane_free + (size_t)(task.b - p.D) * p.Bk + task.idx / S::CT,
+                                       (unsigned)S::NR, err);
             } else {
-                ok = wait_at_least(col_done + task.b, (unsigned)(planes_in<N>(p, task.b) * S::CT), err);
-                ok = ok && wait_at_least(chain + task.idx, (unsigned)task.b, err);
+                ok = wait_at_least(col_done + task.b, (unsigned)(planes_in(p, task.b) * S::CT), err);
             }
             s_ok = ok;
         }
@@ -304,12 +370,17 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused(FusedParams p) {
                 atomicAdd(col_done + task.b, 1u);
             }
         } else {
-            if (s_ok) row_task<N, OBJ>(p, smem, task.b, task.idx, planes_in<N>(p, task.b));
+            if (s_ok) {
+                row_task<N, OBJ>(p, smem, task.b, task.idx, planes_in(p, task.b), plane_free,
+                                 chain, err, &s_ok);
+            } else if (tid == 0) {  // release the planes anyway so that no wait is left behind
+                for (int kk = 0; kk < planes_in(p, task.b); ++kk)
+                    atomicAdd(plane_free + (size_t)task.b * p.Bk + kk, 1u);
+            }
             __syncthreads();
             if (tid == 0) {
                 __threadfence();
                 st_release(chain + task.idx, (unsigned)task.b + 1u);
-                atomicAdd(row_done + task.b, 1u);
             }
         }
     }
@@ -339,15 +410,20 @@ __global__ void __launch_bounds__(1024) k_loss_fused(const double *__restrict__ 
 
 // ---------------------------------------------------------------- host side
 
-size_t fused_sync_words(int N, int n_bf, int Bk) {
-    const int nbatch = (n_bf + Bk - 1) / Bk;
-    const int rt = std::min(kFusedThreads / (N / 8), N);
-    return 2 + 2 * (size_t)nbatch + (size_t)(N / rt);
+static int row_tasks_for(int N) {
+    const int groups = kFusedThreads / (N / kPts);
+    return N / std::min(groups, N);
 }
 
-size_t fused_ring_elems(int N, int Bk) { return (size_t)kRingSlots * Bk * (size_t)N * (N / 2 + 1); }
-size_t fused_hring_elems(int N, int Bk) { return (size_t)kRingSlots * Bk * (size_t)(N / 2 + 1); }
-int fused_row_tasks(int N) { return N / std::min(kFusedThreads / (N / 8), N); }
+size_t fused_sync_words(int N, int n_bf, int Bk) {
+    const int nbatch = (n_bf + Bk - 1) / Bk;
+    return 2 + (size_t)nbatch * (1 + (size_t)Bk) + (size_t)row_tasks_for(N);
+}
+
+static size_t ldz_for(int N) { return (size_t)((N / 2 + 1 + 7) / 8 * 8); }
+size_t fused_ring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)N * ldz_for(N); }
+size_t fused_hring_elems(int N, int Bk, int D) { return (size_t)D * Bk * ldz_for(N); }
+int fused_row_tasks(int N) { return row_tasks_for(N); }
 
 template <int N, bool OBJ>
 static cudaError_t fused_launch(const FusedParams &fp, cudaStream_t s) {
@@ -402,6 +478,7 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     fp.n_bf = a.n_bf;
     fp.Bk = a.Bk;
     fp.nbatch = nbatch;
+    fp.D = a.D;
     fp.tc = make_trial_const(a, th, N);
     e = want_object ? fused_launch<N, true>(fp, s) : fused_launch<N, false>(fp, s);
     if (e != cudaSuccess) return e;

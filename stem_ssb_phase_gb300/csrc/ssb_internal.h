@@ -53,6 +53,7 @@ struct ObjectiveArgs {
     double *S2g;            // per row task sums of phi^2
     unsigned *sync;         // scheduler counters
     int Bk;                 // BF planes per batch
+    int D;                  // ring slots
     int mode;               // 0 SSB2, 1 SSB1
     double step, lam, semi, dalpha;  // geometry (Angstrom, rad)
 };
@@ -65,8 +66,8 @@ cudaError_t launch_theta_tables(const ObjectiveArgs &a, const TrialHost &th, cud
 
 // persistent fused path (SSB2): sizes of its buffers and the evaluation itself
 size_t fused_sync_words(int N, int n_bf, int Bk);
-size_t fused_ring_elems(int N, int Bk);
-size_t fused_hring_elems(int N, int Bk);
+size_t fused_ring_elems(int N, int Bk, int D);
+size_t fused_hring_elems(int N, int Bk, int D);
 int fused_row_tasks(int N);
 cudaError_t run_objective_fused(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,
                                 bool want_object, cudaStream_t s);

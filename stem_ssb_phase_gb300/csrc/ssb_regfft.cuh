@@ -1,14 +1,16 @@
-// Register-resident FFT of length N by a group of T = N/8 threads, each holding 8 points.
+// Register-resident FFT of length N by a group of T = N/E threads, each holding E points
+// (E = 8 or 16; with E = 16 one warp holds a 512-point transform and only warp-level
+// synchronisation is needed).
 //
-// Thread j of the group holds x[j + T r] (r = 0..7) on entry and X[j + T r] on exit
-// (natural order both sides).  Passes follow Stockham's self-sorting schedule (radix 8,
+// Thread j of the group holds x[j + T r] (r = 0..E-1) on entry and X[j + T r] on exit
+// (natural order on both sides).  Passes follow Stockham's self-sorting schedule (radix 8,
 // then a final radix 4 or 2 when log2 N is not a multiple of 3); between passes the
 // points go through a padded shared-memory buffer of N + N/8 complex values per group.
-// With T threads, a radix-R pass has N/R butterflies: butterfly b reads x[b + (N/R) q],
-// twists it by exp(S 2 pi i q (b mod Ns) / (Ns R)), takes the R-point DFT and writes
-// y[(b - b mod Ns) R + b mod Ns + Ns q].  Because thread j's registers hold exactly the
-// inputs of butterflies j + T m, no shuffle is needed, and the last pass leaves its
-// outputs in registers in natural order.
+// A radix-R pass has N/R butterflies: butterfly b reads x[b + (N/R) q], twists it by
+// exp(S 2 pi i q (b mod Ns) / (Ns R)), takes the R-point DFT and writes
+// y[(b - b mod Ns) R + b mod Ns + Ns q].  Thread j runs butterflies b = j + T m,
+// m < E/R, whose inputs are exactly its registers m + (E/R) q, so no shuffle is needed,
+// and the last pass leaves its outputs in registers in natural order.
 #pragma once
 
 #include "ssb_device.cuh"
@@ -16,15 +18,15 @@
 namespace ssb {
 
 // Padded shared-memory index: one spare slot every 8 complex values keeps the pass
-// exchanges free of bank conflicts for 64-bit accesses.
+// exchanges (and twiddle reads) free of most bank conflicts for 64-bit accesses.
 __device__ __forceinline__ int padx(int i) { return i + (i >> 3); }
 
-template <int N>
+template <int N, int E>
 struct RegFFT {
-    static constexpr int T = N / 8;
+    static constexpr int T = N / E;
     static constexpr int SMEM = N + N / 8;  // complex values per group
     static constexpr int LOG2N = N == 32 ? 5 : N == 64 ? 6 : N == 128 ? 7 : N == 256 ? 8 : 9;
-    static constexpr int N8 = LOG2N / 3;       // radix-8 passes
+    static constexpr int N8 = LOG2N / 3;        // radix-8 passes
     static constexpr int TAIL = LOG2N - 3 * N8; // 0, 1 (radix 2) or 2 (radix 4)
 };
 
@@ -49,14 +51,12 @@ __device__ __forceinline__ void dft8(float2 (&v)[8]) {
 }
 
 // One Stockham pass of radix R (8, 4 or 2) over the group's registers, span Ns.
-// If LAST, results stay in registers (natural order); otherwise they are written to sm
-// and read back in the next pass's input order.  bar() synchronises the group.
-template <int N, int R, int S, bool LAST, typename Bar>
-__device__ __forceinline__ void stockham_pass(float2 (&v)[8], float2 *sm, const float2 *tw,
+// twp is the padded twiddle table: twp[padx(m)] = exp(+2 pi i m / N).
+template <int N, int E, int R, int S, bool LAST, typename Bar>
+__device__ __forceinline__ void stockham_pass(float2 (&v)[E], float2 *sm, const float2 *twp,
                                               int j, int Ns, Bar bar) {
-    constexpr int T = N / 8;
-    constexpr int NB = N / R;        // butterflies
-    constexpr int PER = NB / T;      // butterflies per thread (1, 2 or 4)
+    constexpr int T = N / E;
+    constexpr int PER = E / R;  // butterflies per thread
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
         const int b = j + T * m;
@@ -67,7 +67,7 @@ __device__ __forceinline__ void stockham_pass(float2 (&v)[8], float2 *sm, const 
         if (Ns > 1) {
             const int step = N / (Ns * R);
 #pragma unroll
-            for (int q = 1; q < R; ++q) u[q] = cmul(u[q], twid<S>(tw, q * k * step));
+            for (int q = 1; q < R; ++q) u[q] = cmul(u[q], twid<S>(twp, padx(q * k * step)));
         }
         if (R == 8) {
             float2 w[8];
@@ -96,34 +96,34 @@ __device__ __forceinline__ void stockham_pass(float2 (&v)[8], float2 *sm, const 
     if (!LAST) {
         bar();
 #pragma unroll
-        for (int r = 0; r < 8; ++r) v[r] = sm[padx(j + T * r)];
+        for (int r = 0; r < E; ++r) v[r] = sm[padx(j + T * r)];
         bar();
     }
 }
 
-// Full transform.  sm: this group's N + N/8 complex scratch; tw: exp(+2 pi i m/N), m < N.
-template <int N, int S, typename Bar>
-__device__ __forceinline__ void reg_fft(float2 (&v)[8], float2 *sm, const float2 *tw, int j,
+// Full transform.  sm: this group's N + N/8 complex scratch; twp: padded twiddle table.
+template <int N, int E, int S, typename Bar>
+__device__ __forceinline__ void reg_fft(float2 (&v)[E], float2 *sm, const float2 *twp, int j,
                                         Bar bar) {
-    using F = RegFFT<N>;
+    using F = RegFFT<N, E>;
     int Ns = 1;
     if (F::TAIL == 0) {
 #pragma unroll
         for (int p = 0; p < F::N8 - 1; ++p) {
-            stockham_pass<N, 8, S, false>(v, sm, tw, j, Ns, bar);
+            stockham_pass<N, E, 8, S, false>(v, sm, twp, j, Ns, bar);
             Ns *= 8;
         }
-        stockham_pass<N, 8, S, true>(v, sm, tw, j, Ns, bar);
+        stockham_pass<N, E, 8, S, true>(v, sm, twp, j, Ns, bar);
     } else {
 #pragma unroll
         for (int p = 0; p < F::N8; ++p) {
-            stockham_pass<N, 8, S, false>(v, sm, tw, j, Ns, bar);
+            stockham_pass<N, E, 8, S, false>(v, sm, twp, j, Ns, bar);
             Ns *= 8;
         }
         if (F::TAIL == 2)
-            stockham_pass<N, 4, S, true>(v, sm, tw, j, Ns, bar);
+            stockham_pass<N, E, 4, S, true>(v, sm, twp, j, Ns, bar);
         else
-            stockham_pass<N, 2, S, true>(v, sm, tw, j, Ns, bar);
+            stockham_pass<N, E, 2, S, true>(v, sm, twp, j, Ns, bar);
     }
 }
 
