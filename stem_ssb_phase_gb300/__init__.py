@@ -22,8 +22,8 @@ STATUS = {0: "SSB_OK", 1: "SSB_ERR_ARG", 2: "SSB_ERR_UNSUPPORTED", 3: "SSB_ERR_O
 
 # every symbol include/ssb.h declares
 EXPORTS = ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_info", "ssb_export_g",
-           "ssb_unpack_counts", "ssb_profile_objective", "ssb_status_string", "ssb_last_error",
-           "ssb_kernel_launches", "ssb_destroy")
+           "ssb_unpack_counts", "ssb_profile_objective", "ssb_loss_noalloc", "ssb_status_string",
+           "ssb_last_error", "ssb_kernel_launches", "ssb_destroy")
 
 
 class SSBError(RuntimeError):
@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_unpack_counts.argtypes = [vp, i, sz, vp, vp]
     lib.ssb_profile_objective.argtypes = [vp, ctypes.POINTER(_Params), ctypes.POINTER(_KernelTime),
                                           i, ctypes.POINTER(i), vp]
+    lib.ssb_loss_noalloc.argtypes = [ctypes.POINTER(_Geometry), vp, ctypes.POINTER(_Params),
+                                     ctypes.POINTER(ctypes.c_double), vp]
     lib.ssb_status_string.argtypes = [i]
     lib.ssb_status_string.restype = ctypes.c_char_p
     lib.ssb_last_error.argtypes = []
@@ -78,7 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_destroy.argtypes = [vp]
     lib.ssb_destroy.restype = None
     for name in ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_info",
-                 "ssb_export_g", "ssb_unpack_counts", "ssb_profile_objective"):
+                 "ssb_export_g", "ssb_unpack_counts", "ssb_profile_objective", "ssb_loss_noalloc"):
         getattr(lib, name).restype = i
     _lib = lib
     return lib

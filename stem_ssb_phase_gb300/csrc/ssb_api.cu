@@ -25,6 +25,8 @@ void count_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxe
 
 static thread_local std::string g_last_error;
 
+void set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
+
 // ---- per-launch profiler (active only inside ssb_profile_objective) ----
 struct ProfRecord {
     std::string name;

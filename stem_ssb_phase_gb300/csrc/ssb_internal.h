@@ -10,6 +10,9 @@
 
 namespace ssb {
 
+// Records the detail that ssb_last_error() reports on this thread.
+void set_last_error(const char *msg);
+
 // Launch-count bookkeeping (every kernel launch of the library goes through this).
 void count_launch(uint64_t n = 1);
 
