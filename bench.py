@@ -113,18 +113,18 @@ class ClockSampler:
 # ---------------------------------------------------------------- roofline helpers
 
 def _algorithmic_bytes(n_bf: int, n: int) -> dict:
-    """Bytes each kernel must move per objective, by kernel name (the G cache read once;
-    the column-pass intermediate written once and read once where a kernel boundary
-    separates the passes; float64 moment accumulators read and written per BF batch are
-    not counted)."""
+    """Bytes each kernel must move per objective, by kernel name: the G cache read once
+    (n_bf x (N/2+1) x N complex64).  The fused kernel keeps the column-pass intermediate in
+    L2, so the G read is all it must move; the two-kernel SSB1 path also writes and reads
+    the full-plane intermediate once."""
     h = n // 2 + 1
     g = n_bf * h * n * 8
     x = n_bf * n * n * 8
-    return {"k_correct_cols": g + x, "k_rows_moments": x}
+    return {"k_fused": g, "k_correct_cols": g + x, "k_rows_moments": x}
 
 
 def _traffic_record():
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = os.path.join(ROOT, "profiles", "k_fused_counters.json")
     if not os.path.exists(p):
         return {}
     with open(p) as f:
@@ -169,7 +169,11 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.set_device(local_rank)
     w = ssb_synth.WORKLOADS[args.workload]
-    geom, counts, _ = ssb_synth.simulate_counts_torch(w, "cuda")
+    sub = None
+    if args.bf_subset:
+        n_all = ssb_synth.make_geometry(w).n_bf
+        sub = np.linspace(0, n_all - 1, min(args.bf_subset, n_all)).astype(int)
+    geom, counts, _ = ssb_synth.simulate_counts_torch(w, "cuda", geom=ssb_synth.make_geometry(w, bf_subset=sub))
     n = geom.scan_n
     cores = len(os.sched_getaffinity(0))
     sample = None
@@ -236,18 +240,32 @@ def run_ours(args, rank, world, local_rank):
     name, (nl, ms) = top
     total_ms = sum(v[1] for v in prof.values())
     roof = None
+    roof_alu = None
     if name in algo:
         per_launch = algo[name] / nl
         achieved = per_launch / (ms / nl / 1e3) / 1e9
-        rec = _traffic_record().get(name)
+        rec = _traffic_record()
+        fresh = bool(rec) and rec.get("source") == source_digest() and name == rec.get("kernel")
         traffic = None
-        if rec and rec.get("source") == source_digest():
-            traffic = rec.get("bytes_per_launch")
+        if fresh:
+            # ncu counters of a smaller capture, scaled by the BF planes one launch processes
+            traffic = int(rec["dram_bytes_per_plane"] * geom.n_bf * args.trials / nl)
         roof = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": traffic, "algorithmic_bytes_per_launch": int(per_launch),
-                "peak_kind": peak_kind, "launches_per_objective": nl,
+                "peak_kind": peak_kind + " hbm_gbs (copy)", "launches_per_objective": nl,
                 "kernel_share": round(ms / total_ms, 3)}
+        if fresh and clk:
+            # issue-slot roofline: executed warp instructions (ncu, per BF plane) over the
+            # launch time, against 4 issue slots per SM per cycle at the sampled clock
+            inst = rec["warp_inst_per_plane"] * geom.n_bf / nl
+            sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+            ach = inst / (ms / nl / 1e3) / 1e12
+            pk = sms * 4 * clk["sm_mhz"] * 1e6 / 1e12
+            roof_alu = {"bound": "alu", "kernel": name, "achieved": round(ach, 3), "peak": round(pk, 3),
+                        "unit": "Twarp-inst/s", "frac": round(ach / pk, 4),
+                        "peak_kind": "derived: %d SMs x 4 schedulers x 1 warp-instruction/clock x %.0f MHz sampled"
+                                     % (sms, clk["sm_mhz"])}
     objective_bytes = geom.n_bf * (n // 2 + 1) * n * 8
     hbm_g_only = objective_bytes / (ms_per_step / 1e3 / args.trials) / 1e9
 
@@ -278,6 +296,7 @@ def run_ours(args, rank, world, local_rank):
             "e2e": e2e,
             "gpu_launches": int(launches),
             "roofline": roof,
+            "roofline_alu": roof_alu,
             "hbm_fraction_g_only": round(hbm_g_only / peak, 4),
             "kernel_ms_per_objective": {k: round(v[1], 4) for k, v in prof.items()},
             "clocks": clk,
@@ -333,6 +352,8 @@ def main():
     ap.add_argument("--trials", type=int, default=1)
     ap.add_argument("--workload", default="full", choices=sorted(ssb_synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf-subset", type=int, default=0,
+                    help="evenly spaced BF pixels of the workload (profiling a small case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
