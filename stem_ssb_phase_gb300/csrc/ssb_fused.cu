@@ -43,7 +43,7 @@ struct FusedParams {
     const float4 *kgeo;   // per BF (alpha_x, alpha_y, a_k, 0)
     const uint2 *kturn;   // per BF bilinear phase slopes
     const float2 *tw;     // [N] exp(+2 pi i m/N)
-    float2 *Z;            // ring [D][Bk][N][LDZ], rows of the column-pass output
+    float2 *Z;            // ring [D][Bk][H][N]: column-pass output, one column contiguous
     float2 *hrow;         // ring [D][Bk][LDZ], Nyquist-row Hermitian parts
     double *S1;           // [P]
     double *S2g;          // [row tasks]
@@ -64,14 +64,14 @@ struct FusedShape {
     static constexpr int CT = (H + CW - 1) / CW;    // column tasks per plane
     static constexpr int NR = N / RT;               // row tasks per trial
     static constexpr int SMF = RegFFT<N, kPts>::SMEM;  // FFT scratch per group
-    static constexpr int LDZ = (H + 7) / 8 * 8;     // intermediate row stride (64 B multiple)
-    static constexpr int CHUNKS = LDZ / 2;          // 16-byte chunks per row
-    static constexpr int LDS = CW + 1;              // column-task staging stride
+    static constexpr int LDZ = (H + 7) / 8 * 8;     // h row stride (64 B multiple)
+    static constexpr int RC = RT / 2;               // 16-byte chunks per column segment
+    static constexpr int LDC = RT + 2;              // staged column-segment stride (16-B multiple)
     // dynamic shared memory layout, in float2 units
     static constexpr int OFF_TW = 0;                                // padded twiddles
     static constexpr int OFF_FFT = OFF_TW + (N + N / 8 + 2 + 1) / 2 * 2;
-    static constexpr int OFF_TILE = OFF_FFT + GROUPS * SMF;         // [2][RT + 1][LDZ]
-    static constexpr int TILEBUF = (RT + 1) * LDZ;                  // rows, then h
+    static constexpr int OFF_TILE = OFF_FFT + GROUPS * SMF;         // [2][H][LDC] + h
+    static constexpr int TILEBUF = H * LDC + LDZ;                   // segments, then h
     static constexpr int OFF_RED = OFF_TILE + 2 * TILEBUF;
     static constexpr int TOTAL = OFF_RED + 16;  // 8 warp partials (8 bytes each)
     static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float2);
@@ -165,35 +165,29 @@ __device__ void column_task(const FusedParams &p, float2 *smem, int b, int idx) 
         for (int r = 0; r < kPts; ++r) v[r] = make_float2(0.f, 0.f);
     }
     reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
-    // transpose the task's CW columns through shared memory (aliasing the FFT scratch)
-    // so that each output row segment of CW values is written as whole sectors
-    __syncthreads();
-    float2 *stage = smem + S::OFF_FFT;
+    if (valid) {
+        float2 *z = p.Z + (((size_t)slot * p.Bk + kk) * S::H + nx) * N + j;
 #pragma unroll
-    for (int r = 0; r < kPts; ++r) stage[(j + S::T * r) * S::LDS + grp] = v[r];
-    __syncthreads();
-    const int c0 = ct * S::CW;
-    const int ncol = S::H - c0 < S::CW ? S::H - c0 : S::CW;
-    float2 *z = p.Z + ((size_t)slot * p.Bk + kk) * (size_t)N * S::LDZ + c0;
-    for (int e = tid; e < N * S::CW; e += kFusedThreads) {
-        const int ry = e / S::CW, c = e - ry * S::CW;
-        if (c < ncol) __stcg(z + (size_t)ry * S::LDZ + c, stage[ry * S::LDS + c]);
+        for (int r = 0; r < kPts; ++r) __stcg(z + S::T * r, v[r]);
     }
 }
 
 // ---------------------------------------------------------------- row task
 
-// Start the asynchronous copy of one plane's RT rows and its Nyquist terms into buf.
+// Start the asynchronous copy of one plane's RT-row segment of every half-plane column
+// (RT consecutive values, contiguous in the column-major ring) and of its Nyquist terms.
 template <int N>
 __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk, int ry0,
                                           float2 *buf) {
     using S = FusedShape<N>;
-    const float2 *zsrc = p.Z + (((size_t)slot * p.Bk + kk) * N + ry0) * S::LDZ;
-    for (int e = threadIdx.x; e < S::RT * S::CHUNKS; e += kFusedThreads)
-        cp_async16(buf + 2 * e, zsrc + 2 * e);
+    const float2 *zsrc = p.Z + ((size_t)slot * p.Bk + kk) * S::H * N + ry0;
+    for (int e = threadIdx.x; e < S::H * S::RC; e += kFusedThreads) {
+        const int nx = e / S::RC, c = e - nx * S::RC;
+        cp_async16(buf + nx * S::LDC + 2 * c, zsrc + (size_t)nx * N + 2 * c);
+    }
     const float2 *hsrc = p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ;
-    for (int e = threadIdx.x; e < S::CHUNKS; e += kFusedThreads)
-        cp_async16(buf + S::RT * S::LDZ + 2 * e, hsrc + 2 * e);
+    for (int e = threadIdx.x; e < S::LDZ / 2; e += kFusedThreads)
+        cp_async16(buf + S::H * S::LDC + 2 * e, hsrc + 2 * e);
     cp_async_commit();
 }
 
@@ -234,8 +228,8 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             __threadfence();
             atomicAdd(plane_free + (size_t)b * p.Bk + kk, 1u);
         }
-        const float2 *row = cur + lr * S::LDZ;
-        const float2 *hs = cur + S::RT * S::LDZ;
+        const float2 *seg = cur + lr;               // element (nx, lr) at seg[nx * LDC]
+        const float2 *hs = cur + S::H * S::LDC;
         float2 v[kPts];
 #pragma unroll
         for (int r = 0; r < kPts; ++r) {
@@ -243,10 +237,10 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             if (!active) {
                 v[r] = make_float2(0.f, 0.f);
             } else if (nx <= N / 2) {
-                v[r] = row[nx];
+                v[r] = seg[nx * S::LDC];
             } else {
                 const int m = N - nx;
-                const float2 z = row[m];
+                const float2 z = seg[m * S::LDC];
                 const float2 h = hs[m];
                 v[r] = make_float2(fmaf(sgn2, h.x, -z.x), fmaf(-sgn2, h.y, z.y));
             }
@@ -421,7 +415,7 @@ size_t fused_sync_words(int N, int n_bf, int Bk) {
 }
 
 static size_t ldz_for(int N) { return (size_t)((N / 2 + 1 + 7) / 8 * 8); }
-size_t fused_ring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)N * ldz_for(N); }
+size_t fused_ring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)N * (N / 2 + 1); }
 size_t fused_hring_elems(int N, int Bk, int D) { return (size_t)D * Bk * ldz_for(N); }
 int fused_row_tasks(int N) { return row_tasks_for(N); }
 

@@ -65,9 +65,27 @@ __device__ __forceinline__ void stockham_pass(float2 (&v)[E], float2 *sm, const 
 #pragma unroll
         for (int q = 0; q < R; ++q) u[q] = v[m + PER * q];
         if (Ns > 1) {
-            const int step = N / (Ns * R);
-#pragma unroll
-            for (int q = 1; q < R; ++q) u[q] = cmul(u[q], twid<S>(twp, padx(q * k * step)));
+            // one table read, the other twiddles as products of it (depth 3 for radix 8)
+            const float2 w1 = twid<S>(twp, padx(k * (N / (Ns * R))));
+            if (R == 2) {
+                u[1] = cmul(u[1], w1);
+            } else {
+                const float2 w2 = cmul(w1, w1);
+                const float2 w3 = cmul(w2, w1);
+                u[1] = cmul(u[1], w1);
+                u[2] = cmul(u[2], w2);
+                u[3] = cmul(u[3], w3);
+                if (R == 8) {
+                    const float2 w4 = cmul(w2, w2);
+                    const float2 w5 = cmul(w4, w1);
+                    const float2 w6 = cmul(w3, w3);
+                    const float2 w7 = cmul(w4, w3);
+                    u[4] = cmul(u[4], w4);
+                    u[5] = cmul(u[5], w5);
+                    u[6] = cmul(u[6], w6);
+                    u[7] = cmul(u[7], w7);
+                }
+            }
         }
         if (R == 8) {
             float2 w[8];
