@@ -106,7 +106,7 @@ struct ssb_ctx {
     double2 *Osum = nullptr;
     double *loss = nullptr;
     int loss_cap = 0;
-    float2 *Zring = nullptr, *hring = nullptr;
+    float2 *Zring = nullptr, *hring = nullptr, *rring = nullptr;
     double *S2g = nullptr;
     unsigned *sync = nullptr;
     int Bk = 0, D = 0;
@@ -132,6 +132,7 @@ struct ssb_ctx {
         a.loss = loss;
         a.Zring = Zring;
         a.hring = hring;
+        a.rring = rring;
         a.S2g = S2g;
         a.sync = sync;
         a.Bk = Bk;
@@ -148,7 +149,7 @@ struct ssb_ctx {
 static void free_ctx(ssb_ctx *c) {
     if (!c) return;
     void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->X, c->S1, c->S2,
-                    c->Osum, c->loss, c->flag, c->Zring, c->hring, c->S2g, c->sync};
+                    c->Osum, c->loss, c->flag, c->Zring, c->hring, c->rring, c->S2g, c->sync};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete c;
@@ -282,6 +283,7 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     if (c->fused) {
         SSB_ALLOC(c->Zring, fused_ring_elems(N, c->Bk, c->D), sb);
         SSB_ALLOC(c->hring, fused_hring_elems(N, c->Bk, c->D), sb);
+        SSB_ALLOC(c->rring, fused_rring_elems(N, c->Bk, c->D), sb);
         SSB_ALLOC(c->S2g, (size_t)fused_row_tasks(N), sb);
         SSB_ALLOC(c->sync, fused_sync_words(N, c->n_bf, c->Bk), sb);
     } else {

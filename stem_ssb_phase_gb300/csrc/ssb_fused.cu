@@ -45,10 +45,12 @@ struct FusedParams {
     const float2 *tw;     // [N] exp(+2 pi i m/N)
     float2 *Z;            // ring [D][Bk][H][N]: column-pass output, one column contiguous
     float2 *hrow;         // ring [D][Bk][LDZ], Nyquist-row Hermitian parts
+    float2 *rrow;         // ring [D][Bk][N/2]: Rp(2j) + i Rp(2j+1), Rp the Nyquist-row term
     double *S1;           // [P]
     double *S2g;          // [row tasks]
     double2 *Osum;        // [P] (object redraw only)
-    unsigned *sync;       // ticket, error, col_done[nbatch], plane_free[nbatch][Bk], chain[row tasks]
+    unsigned *sync;       // ticket, error, col_done[nbatch], plane_free[nbatch][Bk],
+                          // h_cnt[nbatch][Bk], chain[row tasks]
     int n_bf, Bk, nbatch;
     int D;                // ring slots (batches in flight)
     TrialConst tc;
@@ -59,6 +61,7 @@ struct FusedShape {
     static constexpr int T = N / kPts;              // threads per transform
     static constexpr int GROUPS = kFusedThreads / T;  // transforms per block
     static constexpr int H = N / 2 + 1;             // half-plane columns
+    static constexpr int M = N / 2;                 // row transforms: M-point complex IFFT
     static constexpr int CW = GROUPS;               // columns per column task
     static constexpr int RT = GROUPS < N ? GROUPS : N;  // rows per row task (multiple of 4)
     static constexpr int CT = (H + CW - 1) / CW;    // column tasks per plane
@@ -69,9 +72,10 @@ struct FusedShape {
     static constexpr int LDC = RT + 2;              // staged column-segment stride (16-B multiple)
     // dynamic shared memory layout, in float2 units
     static constexpr int OFF_TW = 0;                                // padded twiddles
-    static constexpr int OFF_FFT = OFF_TW + (N + N / 8 + 2 + 1) / 2 * 2;
+    static constexpr int OFF_TW2 = OFF_TW + (N + N / 8 + 2 + 1) / 2 * 2;  // M-point table
+    static constexpr int OFF_FFT = OFF_TW2 + (M + M / 8 + 2 + 1) / 2 * 2;
     static constexpr int OFF_TILE = OFF_FFT + GROUPS * SMF;         // [2][H][LDC] + h
-    static constexpr int TILEBUF = H * LDC + LDZ;                   // segments, then h
+    static constexpr int TILEBUF = H * LDC + LDZ + M;               // segments, h, Rp
     static constexpr int OFF_RED = OFF_TILE + 2 * TILEBUF;
     static constexpr int TOTAL = OFF_RED + 16;  // 8 warp partials (8 bytes each)
     static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float2);
@@ -115,8 +119,37 @@ __device__ __forceinline__ void warp_bar() { __syncwarp(); }
 
 // ---------------------------------------------------------------- column task
 
+// Rp(rx) = 2 Re sum_{0 < nx < N/2} h(nx) e^{2 pi i nx rx / N}, the Nyquist-row contribution
+// to Re c (times (-1)^ry), as one N/2-point complex IFFT of the packed real-output form;
+// stored as Rp(2j) + i Rp(2j+1).  Run by one group of T threads.
+// Every lane of the calling warp must call it (the transform synchronises the warp);
+// only the group with store = true writes the result.
 template <int N>
-__device__ void column_task(const FusedParams &p, float2 *smem, int b, int idx) {
+__device__ void nyquist_transform(const FusedParams &p, float2 *fsm, const float2 *twN,
+                                  const float2 *twM, int slot, int kk, int j, bool store) {
+    using S = FusedShape<N>;
+    const float2 *h = p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ;
+    float2 v[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int m = j + S::T * r, mc = S::M - m;
+        const float2 hm = (m >= 1) ? __ldcg(h + m) : make_float2(0.f, 0.f);
+        const float2 hc = (mc >= 1 && mc < S::M) ? __ldcg(h + mc) : make_float2(0.f, 0.f);
+        const float2 a = make_float2(hm.x + hc.x, hm.y - hc.y);
+        const float2 bb = cmul(make_float2(hm.x - hc.x, hm.y + hc.y), twid<+1>(twN, padx(m)));
+        v[r] = make_float2(a.x - bb.y, a.y + bb.x);
+    }
+    reg_fft<S::M, 8, +1>(v, fsm, twM, j, warp_bar);
+    if (store) {
+        float2 *out = p.rrow + ((size_t)slot * p.Bk + kk) * S::M + j;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) __stcg(out + S::T * r, v[r]);
+    }
+}
+
+template <int N>
+__device__ void column_task(const FusedParams &p, float2 *smem, int b, int idx, unsigned *h_cnt,
+                            unsigned *err, int *s_ok) {
     using S = FusedShape<N>;
     const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
     const int kk = idx / S::CT, ct = idx - kk * S::CT;
@@ -170,12 +203,31 @@ __device__ void column_task(const FusedParams &p, float2 *smem, int b, int idx) 
 #pragma unroll
         for (int r = 0; r < kPts; ++r) __stcg(z + S::T * r, v[r]);
     }
+    // Once every column task of the plane has written its Nyquist terms, the plane's last
+    // column task transforms them with its last warp, whose groups are all idle there (the
+    // last task holds at most one warp's worth of valid columns for every supported N).
+    __syncthreads();
+    unsigned *hc = h_cnt + (size_t)b * p.Bk + kk;
+    if (tid == 0) {
+        __threadfence();
+        atomicAdd(hc, 1u);
+    }
+    if (ct == S::CT - 1) {
+        if (tid == 0) *s_ok = wait_at_least(hc, (unsigned)S::CT, err);
+        __syncthreads();
+        static_assert(S::H - (S::CT - 1) * S::CW <= S::CW - 32 / S::T,
+                      "the last column task must leave its last warp idle");
+        if (tid >= kFusedThreads - 32 && *s_ok)  // whole warp: the transform syncs the warp
+            nyquist_transform<N>(p, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW,
+                                 smem + S::OFF_TW2, slot, kk, j, grp == S::GROUPS - 1);
+    }
 }
 
 // ---------------------------------------------------------------- row task
 
 // Start the asynchronous copy of one plane's RT-row segment of every half-plane column
-// (RT consecutive values, contiguous in the column-major ring) and of its Nyquist terms.
+// (RT consecutive values, contiguous in the column-major ring), of its Nyquist terms h
+// and of its Nyquist-row transform Rp.
 template <int N>
 __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk, int ry0,
                                           float2 *buf) {
@@ -188,9 +240,18 @@ __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk
     const float2 *hsrc = p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ;
     for (int e = threadIdx.x; e < S::LDZ / 2; e += kFusedThreads)
         cp_async16(buf + S::H * S::LDC + 2 * e, hsrc + 2 * e);
+    const float2 *rsrc = p.rrow + ((size_t)slot * p.Bk + kk) * S::M;
+    for (int e = threadIdx.x; e < S::M / 2; e += kFusedThreads)
+        cp_async16(buf + S::H * S::LDC + S::LDZ + 2 * e, rsrc + 2 * e);
     cp_async_commit();
 }
 
+// Row ry of the corrected image, split by symmetry (exact):
+//   Im c = real IFFT of Y(m) = -i (Z(m) - s h(m)) (0 < m < N/2), Y(0) = Im Z(0),
+//          Y(N/2) = Im Z(N/2), done as one N/2-point complex IFFT of
+//          V(m) = Y(m) + conj Y(N/2-m) + i (Y(m) - conj Y(N/2-m)) e^{2 pi i m/N},
+//          whose output holds Im c at pixels 2j (real part) and 2j+1 (imaginary part);
+//   Re c = Re Z(0) + (-1)^rx Re Z(N/2) + s Rp(rx),   s = (-1)^ry.
 template <int N, bool OBJ>
 __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int planes,
                          unsigned *plane_free, unsigned *chain, unsigned *err, int *s_ok) {
@@ -201,13 +262,14 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
     const bool active = grp < S::RT;                // N = 32 leaves some groups idle
     const int lr = active ? grp : 0;
     const int ry = ry0 + lr;
-    const float sgn2 = (ry & 1) ? -2.0f : 2.0f;     // 2 (-1)^ry
+    const float sg = (ry & 1) ? -1.0f : 1.0f;       // (-1)^ry
+    const float2 *twN = smem + S::OFF_TW;
     float2 *tiles = smem + S::OFF_TILE;
-    float acc1[kPts];
-    float2 acco[kPts];
+    float acc1[2 * 8];
+    float2 acco[2 * 8];
     float acc2 = 0.f;
 #pragma unroll
-    for (int r = 0; r < kPts; ++r) {
+    for (int r = 0; r < 16; ++r) {
         acc1[r] = 0.f;
         acco[r] = make_float2(0.f, 0.f);
     }
@@ -230,28 +292,41 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         }
         const float2 *seg = cur + lr;               // element (nx, lr) at seg[nx * LDC]
         const float2 *hs = cur + S::H * S::LDC;
-        float2 v[kPts];
+        const float2 *rp = hs + S::LDZ;
+        const float2 z0 = seg[0], zm = seg[S::M * S::LDC];
+        float2 v[8];
 #pragma unroll
-        for (int r = 0; r < kPts; ++r) {
-            const int nx = j + S::T * r;
-            if (!active) {
-                v[r] = make_float2(0.f, 0.f);
-            } else if (nx <= N / 2) {
-                v[r] = seg[nx * S::LDC];
+        for (int r = 0; r < 8; ++r) {
+            const int m = j + S::T * r, mc = S::M - m;
+            float2 ym, yc;
+            if (m == 0) {
+                ym = make_float2(z0.y, 0.f);
+                yc = make_float2(zm.y, 0.f);
             } else {
-                const int m = N - nx;
-                const float2 z = seg[m * S::LDC];
-                const float2 h = hs[m];
-                v[r] = make_float2(fmaf(sgn2, h.x, -z.x), fmaf(-sgn2, h.y, z.y));
+                const float2 za = seg[m * S::LDC], ha = hs[m];
+                const float2 zb = seg[mc * S::LDC], hb = hs[mc];
+                ym = make_float2(fmaf(-sg, ha.y, za.y), fmaf(sg, ha.x, -za.x));
+                yc = make_float2(fmaf(-sg, hb.y, zb.y), fmaf(sg, hb.x, -zb.x));
             }
+            const float2 a = make_float2(ym.x + yc.x, ym.y - yc.y);
+            const float2 bb = cmul(make_float2(ym.x - yc.x, ym.y + yc.y), twid<+1>(twN, padx(m)));
+            v[r] = active ? make_float2(a.x - bb.y, a.y + bb.x) : make_float2(0.f, 0.f);
         }
-        reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
+        reg_fft<S::M, 8, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW2, j, warp_bar);
+        const float re_even = z0.x + zm.x, re_odd = z0.x - zm.x;
 #pragma unroll
-        for (int r = 0; r < kPts; ++r) {
-            const float phi = fast_atan2(v[r].y, v[r].x);
-            acc1[r] += phi;
-            acc2 = fmaf(phi, phi, acc2);
-            if (OBJ) acco[r] = cadd(acco[r], v[r]);
+        for (int r = 0; r < 8; ++r) {
+            const float2 rpv = rp[j + S::T * r];
+            const float re0 = fmaf(sg, rpv.x, re_even), re1 = fmaf(sg, rpv.y, re_odd);
+            const float p0 = fast_atan2(v[r].x, re0), p1 = fast_atan2(v[r].y, re1);
+            acc1[2 * r] += p0;
+            acc1[2 * r + 1] += p1;
+            acc2 = fmaf(p0, p0, acc2);
+            acc2 = fmaf(p1, p1, acc2);
+            if (OBJ) {
+                acco[2 * r] = cadd(acco[2 * r], make_float2(re0, v[r].x));
+                acco[2 * r + 1] = cadd(acco[2 * r + 1], make_float2(re1, v[r].y));
+            }
         }
     }
     // Add this batch into the float64 accumulators.  Only this update is ordered: it
@@ -261,12 +336,15 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
     __syncthreads();
     if (active && *s_ok) {
 #pragma unroll
-        for (int r = 0; r < kPts; ++r) {
-            const size_t i = (size_t)ry * N + j + S::T * r;
-            p.S1[i] = __ldcg(p.S1 + i) + (double)acc1[r];
-            if (OBJ) {
-                const double2 o = __ldcg(p.Osum + i);
-                p.Osum[i] = make_double2(o.x + acco[r].x, o.y + acco[r].y);
+        for (int r = 0; r < 8; ++r) {
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const size_t i = (size_t)ry * N + 2 * (j + S::T * r) + e2;
+                p.S1[i] = __ldcg(p.S1 + i) + (double)acc1[2 * r + e2];
+                if (OBJ) {
+                    const double2 o = __ldcg(p.Osum + i);
+                    p.Osum[i] = make_double2(o.x + acco[2 * r + e2].x, o.y + acco[2 * r + e2].y);
+                }
             }
         }
     }
@@ -333,11 +411,13 @@ __global__ void __launch_bounds__(kFusedThreads, 2) k_fused(FusedParams p) {
     __shared__ int s_ok;
     const int tid = threadIdx.x;
     for (int i = tid; i < N; i += kFusedThreads) smem[S::OFF_TW + padx(i)] = p.tw[i];
+    for (int i = tid; i < S::M; i += kFusedThreads) smem[S::OFF_TW2 + padx(i)] = p.tw[2 * i];
     unsigned *ticket = p.sync;
     unsigned *err = p.sync + 1;
     unsigned *col_done = p.sync + 2;
     unsigned *plane_free = col_done + p.nbatch;
-    unsigned *chain = plane_free + (size_t)p.nbatch * p.Bk;
+    unsigned *h_cnt = plane_free + (size_t)p.nbatch * p.Bk;
+    unsigned *chain = h_cnt + (size_t)p.nbatch * p.Bk;
     __syncthreads();
     while (true) {
         if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
@@ -357,7 +437,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) k_fused(FusedParams p) {
         }
         __syncthreads();
         if (task.kind == 0) {
-            if (s_ok) column_task<N>(p, smem, task.b, task.idx);
+            if (s_ok) column_task<N>(p, smem, task.b, task.idx, h_cnt, err, &s_ok);
             __syncthreads();
             if (tid == 0) {
                 __threadfence();
@@ -411,12 +491,13 @@ static int row_tasks_for(int N) {
 
 size_t fused_sync_words(int N, int n_bf, int Bk) {
     const int nbatch = (n_bf + Bk - 1) / Bk;
-    return 2 + (size_t)nbatch * (1 + (size_t)Bk) + (size_t)row_tasks_for(N);
+    return 2 + (size_t)nbatch * (1 + 2 * (size_t)Bk) + (size_t)row_tasks_for(N);
 }
 
 static size_t ldz_for(int N) { return (size_t)((N / 2 + 1 + 7) / 8 * 8); }
 size_t fused_ring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)N * (N / 2 + 1); }
 size_t fused_hring_elems(int N, int Bk, int D) { return (size_t)D * Bk * ldz_for(N); }
+size_t fused_rring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)(N / 2); }
 int fused_row_tasks(int N) { return row_tasks_for(N); }
 
 template <int N, bool OBJ>
@@ -465,6 +546,7 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     fp.tw = a.tw;
     fp.Z = a.Zring;
     fp.hrow = a.hring;
+    fp.rrow = a.rring;
     fp.S1 = a.S1;
     fp.S2g = a.S2g;
     fp.Osum = a.Osum;

@@ -53,6 +53,7 @@ struct ObjectiveArgs {
     // fused (persistent) path
     float2 *Zring;          // column-pass intermediate ring
     float2 *hring;          // Nyquist-row Hermitian parts ring
+    float2 *rring;          // Nyquist-row transforms ring
     double *S2g;            // per row task sums of phi^2
     unsigned *sync;         // scheduler counters
     int Bk;                 // BF planes per batch
@@ -71,6 +72,7 @@ cudaError_t launch_theta_tables(const ObjectiveArgs &a, const TrialHost &th, cud
 size_t fused_sync_words(int N, int n_bf, int Bk);
 size_t fused_ring_elems(int N, int Bk, int D);
 size_t fused_hring_elems(int N, int Bk, int D);
+size_t fused_rring_elems(int N, int Bk, int D);
 int fused_row_tasks(int N);
 cudaError_t run_objective_fused(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,
                                 bool want_object, cudaStream_t s);

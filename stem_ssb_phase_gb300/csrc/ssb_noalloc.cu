@@ -48,7 +48,7 @@ static cudaError_t scratch_base(unsigned char **out) {
 }
 
 struct NoallocLayout {
-    size_t E, S1, Z, h, S2g, kgeo, kalpha, kturn, yx, tw, loss, sync, total;
+    size_t E, S1, Z, h, rp, S2g, kgeo, kalpha, kturn, yx, tw, loss, sync, total;
 };
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -62,6 +62,7 @@ static NoallocLayout noalloc_layout(int N, int n_bf) {
     L.S1 = o;     o = up256(o + P * sizeof(double));
     L.Z = o;      o = up256(o + fused_ring_elems(N, bk, kNoallocRing) * sizeof(float2));
     L.h = o;      o = up256(o + fused_hring_elems(N, bk, kNoallocRing) * sizeof(float2));
+    L.rp = o;     o = up256(o + fused_rring_elems(N, bk, kNoallocRing) * sizeof(float2));
     L.S2g = o;    o = up256(o + (size_t)fused_row_tasks(N) * sizeof(double));
     L.kgeo = o;   o = up256(o + (size_t)n_bf * sizeof(float4));
     L.kalpha = o; o = up256(o + (size_t)n_bf * sizeof(double2));
@@ -149,6 +150,7 @@ extern "C" ssb_status ssb_loss_noalloc(const ssb_geometry *g, const void *g_cach
     a.loss = (double *)(base + L.loss);
     a.Zring = (float2 *)(base + L.Z);
     a.hring = (float2 *)(base + L.h);
+    a.rring = (float2 *)(base + L.rp);
     a.S2g = (double *)(base + L.S2g);
     a.sync = (unsigned *)(base + L.sync);
     a.Bk = g->n_bf < kNoallocBk ? g->n_bf : kNoallocBk;

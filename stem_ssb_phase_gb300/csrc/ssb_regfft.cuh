@@ -25,7 +25,7 @@ template <int N, int E>
 struct RegFFT {
     static constexpr int T = N / E;
     static constexpr int SMEM = N + N / 8;  // complex values per group
-    static constexpr int LOG2N = N == 32 ? 5 : N == 64 ? 6 : N == 128 ? 7 : N == 256 ? 8 : 9;
+    static constexpr int LOG2N = N == 16 ? 4 : N == 32 ? 5 : N == 64 ? 6 : N == 128 ? 7 : N == 256 ? 8 : 9;
     static constexpr int N8 = LOG2N / 3;        // radix-8 passes
     static constexpr int TAIL = LOG2N - 3 * N8; // 0, 1 (radix 2) or 2 (radix 4)
 };
