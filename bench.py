@@ -140,6 +140,24 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+# ---------------------------------------------------------------- multi-rank helpers
+
+def max_over_ranks(value: float, world: int, device: str = "cpu") -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, units_per_step: float, seconds: float) -> float:
+    """Whole-job units per second: every rank runs `steps` steps of `units_per_step`."""
+    return world * steps * units_per_step / seconds
+
+
 # ---------------------------------------------------------------- CPU oracle baseline
 
 def cpu_oracle_run(geom, counts_sample, theta, workers: int):
@@ -208,13 +226,9 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     clk = clocks.stop()
     launches = ssbgpu.kernel_launches() - l0
-    t_dev = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        tt = torch.tensor([t_dev], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_dev = float(tt.item())
+    t_dev = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, "cuda")
     units = geom.n_bf * n * n * args.trials
-    value = world * args.steps * units / t_dev
+    value = job_throughput(world, args.steps, units, t_dev)
     ms_per_step = 1e3 * t_dev / args.steps
 
     # ---- end to end through the public API: host theta in, host losses out
@@ -224,12 +238,8 @@ def run_ours(args, rank, world, local_rank):
     h0 = time.perf_counter()
     for _ in range(args.steps):
         ctx.loss_batch(thetas)
-    t_e2e = time.perf_counter() - h0
-    if world > 1:
-        tt = torch.tensor([t_e2e], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
-    e2e = {"value": world * args.steps * units / t_e2e, "unit": UNIT,
+    t_e2e = max_over_ranks(time.perf_counter() - h0, world, "cuda")
+    e2e = {"value": job_throughput(world, args.steps, units, t_e2e), "unit": UNIT,
            "h2d_bytes_per_step": 32 * args.trials, "d2h_bytes_per_step": 8 * args.trials}
 
     # ---- per-kernel device times of one objective (events on the library's stream)

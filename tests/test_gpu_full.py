@@ -1,0 +1,55 @@
+"""Parity at the full size the benchmark times: 512 x 512 scan, 192 x 192 detector, all
+8,937 BF pixels, uint32 counts (mean 1,000), generated on the GPU exactly as bench.py
+does, evaluated through the C ABI in the benchmark's launch configuration, and compared
+with the float64 oracle run over every BF pixel in spawned processes on the host cores.
+
+Tolerances as for the other parity tests: loss within 1e-5 relative, mean phase within
+1e-4 rad off the atan2 branch cut."""
+import numpy as np
+import pytest
+
+import oracle
+import ssb_synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def full_case():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from stem_ssb_phase_gb300 import build
+    build.build()
+    import stem_ssb_phase_gb300 as m
+    w = ssb_synth.WORKLOADS["full"]
+    geom, counts, _ = ssb_synth.simulate_counts_torch(w, "cuda")
+    host = counts.cpu().numpy().view(np.uint32)
+    ctx = m.SSB(geom, counts)
+    del counts
+    torch.cuda.empty_cache()
+    yield w, geom, host, ctx
+    ctx.close()
+
+
+def test_full_size_loss_and_mean_phase_match_the_oracle(full_case):
+    w, geom, host, ctx = full_case
+    theta = ssb_synth.draw_trials(w, 1)[0]  # the trial the benchmark times
+    mp, _, loss = ctx.reconstruct(theta, want_object=False)
+    ref = oracle.objective(geom, theta, counts=host, workers=min(32, oracle.default_workers()))
+    assert abs(loss - ref["loss"]) <= 1e-5 * ref["loss"], (loss, ref["loss"])
+    mask = ~ref["branch_cut"]
+    err = np.abs(mp.cpu().numpy().astype(np.float64) - ref["mean_phase"])[mask]
+    assert mask.mean() > 0.9
+    assert err.max() <= 1e-4, (err.max(), int((err > 1e-4).sum()))
+
+
+def test_full_size_batch_equals_scalar_calls(full_case):
+    w, geom, host, ctx = full_case
+    thetas = np.vstack([np.array(w.truth)[None], ssb_synth.draw_trials(w, 2, seed=9)])
+    batch = ctx.loss_batch(thetas)
+    singles = np.array([ctx.loss(t) for t in thetas])
+    assert np.array_equal(batch, singles)
+    assert np.array_equal(ctx.loss_batch(thetas), batch)  # run to run
+    # the generating aberrations give the smallest loss of the three
+    assert int(np.argmin(batch)) == 0
