@@ -33,7 +33,11 @@
 
 namespace ssb {
 
-constexpr int kFusedThreads = 256;
+#ifndef SSB_FUSED_THREADS
+#define SSB_FUSED_THREADS 256
+#endif
+constexpr int kFusedThreads = SSB_FUSED_THREADS;  // threads per block (4 or 8 warps)
+constexpr int kFusedBlocksPerSM = 512 / kFusedThreads;
 constexpr int kPts = 16;                    // points per thread in every transform
 constexpr unsigned kWaitLimit = 1u << 24;  // polls of ~0.1-1 us each before giving up
 
@@ -70,14 +74,20 @@ struct FusedShape {
     static constexpr int LDZ = (H + 7) / 8 * 8;     // h row stride (64 B multiple)
     static constexpr int RC = RT / 2;               // 16-byte chunks per column segment
     static constexpr int LDC = RT + 2;              // staged column-segment stride (16-B multiple)
-    // dynamic shared memory layout, in float2 units
+    // dynamic shared memory layout, in float2 units.  A block runs one task at a time, so
+    // the column task's FFT scratch and the row task's scratch + staged planes share OFF_U.
+    static constexpr int SMR = RegFFT<M, 8>::SMEM;                  // row FFT scratch per group
     static constexpr int OFF_TW = 0;                                // padded twiddles
     static constexpr int OFF_TW2 = OFF_TW + (N + N / 8 + 2 + 1) / 2 * 2;  // M-point table
-    static constexpr int OFF_FFT = OFF_TW2 + (M + M / 8 + 2 + 1) / 2 * 2;
-    static constexpr int OFF_TILE = OFF_FFT + GROUPS * SMF;         // [2][H][LDC] + h
+    static constexpr int OFF_RED = OFF_TW2 + (M + M / 8 + 2 + 1) / 2 * 2;  // warp partials
+    static constexpr int OFF_U = OFF_RED + 16;
+    static constexpr int OFF_FFT = OFF_U;                           // column task: [GROUPS][SMF]
+    static constexpr int OFF_RFFT = OFF_U;                          // row task: [GROUPS][SMR]
+    static constexpr int OFF_TILE = OFF_RFFT + (GROUPS * SMR + 1) / 2 * 2;  // [2][TILEBUF]
     static constexpr int TILEBUF = H * LDC + LDZ + M;               // segments, h, Rp
-    static constexpr int OFF_RED = OFF_TILE + 2 * TILEBUF;
-    static constexpr int TOTAL = OFF_RED + 16;  // 8 warp partials (8 bytes each)
+    static constexpr int U_COL = GROUPS * SMF;
+    static constexpr int U_ROW = OFF_TILE - OFF_U + 2 * TILEBUF;
+    static constexpr int TOTAL = OFF_U + (U_COL > U_ROW ? U_COL : U_ROW);
     static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float2);
 };
 
@@ -94,6 +104,10 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int K>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory"); }
+
+__device__ __forceinline__ void red_relaxed_add(unsigned *p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -209,7 +223,7 @@ __device__ void column_task(const FusedParams &p, float2 *smem, int b, int idx, 
     __syncthreads();
     unsigned *hc = h_cnt + (size_t)b * p.Bk + kk;
     if (tid == 0) {
-        __threadfence();
+        __threadfence();  // publishes this task's ring columns and h values
         atomicAdd(hc, 1u);
     }
     if (ct == S::CT - 1) {
@@ -285,10 +299,10 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         }
         __syncthreads();  // plane kk has landed for every thread
         if (tid == 0) {
-            // this task no longer needs plane kk of the slot: columns of batch b + D may
-            // overwrite it once every row task has passed it
-            __threadfence();
-            atomicAdd(plane_free + (size_t)b * p.Bk + kk, 1u);
+            // This task no longer needs plane kk of the slot: columns of batch b + D may
+            // overwrite it once every row task has passed it.  The plane's reads have all
+            // completed (their data is in shared memory), so no fence is needed here.
+            red_relaxed_add(plane_free + (size_t)b * p.Bk + kk, 1u);
         }
         const float2 *seg = cur + lr;               // element (nx, lr) at seg[nx * LDC]
         const float2 *hs = cur + S::H * S::LDC;
@@ -312,7 +326,7 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             const float2 bb = cmul(make_float2(ym.x - yc.x, ym.y + yc.y), twid<+1>(twN, padx(m)));
             v[r] = active ? make_float2(a.x - bb.y, a.y + bb.x) : make_float2(0.f, 0.f);
         }
-        reg_fft<S::M, 8, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW2, j, warp_bar);
+        reg_fft<S::M, 8, +1>(v, smem + S::OFF_RFFT + grp * S::SMR, smem + S::OFF_TW2, j, warp_bar);
         const float re_even = z0.x + zm.x, re_odd = z0.x - zm.x;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
@@ -348,7 +362,7 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             }
         }
     }
-    // sum of phi^2: warp shuffles, then the 8 warp partials in a fixed order
+    // sum of phi^2: warp shuffles, then the warp partials in a fixed order
     double w2 = active ? (double)acc2 : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) w2 += __shfl_down_sync(0xffffffffu, w2, o);
@@ -404,7 +418,7 @@ __device__ Task decode_ticket(const FusedParams &p, unsigned t) {
 }
 
 template <int N, bool OBJ>
-__global__ void __launch_bounds__(kFusedThreads, 2) k_fused(FusedParams p) {
+__global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(FusedParams p) {
     using S = FusedShape<N>;
     extern __shared__ __align__(16) float2 smem[];
     __shared__ unsigned s_ticket;
