@@ -317,6 +317,60 @@ def run_ours(args, rank, world, local_rank):
     ctx.close()
 
 
+def run_fit(args):
+    """Full fit workload: 200 random trials in one ssb_loss_batch, then 34 sequential
+    scalar evaluations driven by a Nelder-Mead simplex on (C10, |C12|, phi12) from the best
+    trial (rotation held), then the object redraw at the result; end-to-end wall time."""
+    import torch
+    from scipy.optimize import minimize
+
+    import stem_ssb_phase_gb300 as ssbgpu
+    from stem_ssb_phase_gb300 import build as _build
+    _build.build()
+    w = ssb_synth.WORKLOADS["full"]
+    geom, counts, _ = ssb_synth.simulate_counts_torch(w, "cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ctx = ssbgpu.SSB(geom, counts)
+    torch.cuda.synchronize()
+    t_prep = time.perf_counter() - t0
+    del counts
+    torch.cuda.empty_cache()
+    ctx.loss_batch(ssb_synth.draw_trials(w, 2))  # warm-up outside the timed fit
+    l0 = ssbgpu.kernel_launches()
+    t0 = time.perf_counter()
+    trials = ssb_synth.draw_trials(w, 200, seed=104)
+    losses = ctx.loss_batch(trials)
+    best = trials[int(np.argmin(losses))]
+    t_search = time.perf_counter() - t0
+    evals = []
+
+    def f(x):
+        th = (x[0], abs(x[1]), x[2], best[3])
+        v = ctx.loss(th)
+        evals.append(v)
+        return v
+
+    res = minimize(f, best[:3], method="Nelder-Mead",
+                   options={"maxfev": 34, "initial_simplex": None, "xatol": 1e-3, "fatol": 3e-6})
+    t_nm = time.perf_counter() - t0 - t_search
+    theta = (res.x[0], abs(res.x[1]), res.x[2], best[3])
+    mp, obj, loss = ctx.reconstruct(theta, want_object=True)
+    torch.cuda.synchronize()
+    t_total = time.perf_counter() - t0
+    out = {"metric": "full fit workload, end to end (200-trial batch + Nelder-Mead + redraw)",
+           "value": t_total, "unit": "s", "higher_is_better": False, "n_gpus": 1,
+           "dtype": "f32", "data": "synthetic",
+           "config": {"workload": "full: 512x512 scan, 192x192 detector, %d BF" % geom.n_bf,
+                      "trials": 200, "nelder_mead_evaluations": len(evals)},
+           "search_s": t_search, "nelder_mead_s": t_nm, "prepare_s": t_prep,
+           "gpu_launches": ssbgpu.kernel_launches() - l0,
+           "best_trial": [float(x) for x in best], "fit_theta": [float(x) for x in theta],
+           "truth": list(w.truth), "fit_loss": float(loss)}
+    print(json.dumps(out), flush=True)
+    ctx.close()
+
+
 def run_reference(args, rank, world):
     """The float64 CPU oracle on a bounded BF sample of the same workload."""
     if rank != 0:
@@ -362,6 +416,8 @@ def main():
     ap.add_argument("--trials", type=int, default=1)
     ap.add_argument("--workload", default="full", choices=sorted(ssb_synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fit", action="store_true",
+                    help="time the full fit workload (200 trials + Nelder-Mead + redraw) instead")
     ap.add_argument("--bf-subset", type=int, default=0,
                     help="evenly spaced BF pixels of the workload (profiling a small case)")
     args = ap.parse_args()
@@ -378,7 +434,10 @@ def main():
             torch.cuda.set_device(local_rank)
         dist.init_process_group(backend=backend)
     try:
-        if args.impl == "reference":
+        if args.fit:
+            if rank == 0:
+                run_fit(args)
+        elif args.impl == "reference":
             run_reference(args, rank, world)
         else:
             run_ours(args, rank, world, local_rank)
