@@ -18,13 +18,18 @@
 //
 // Tasks (ticket order, phase p = [columns of batch p, rows of batch p-1]):
 //   column task (batch b, plane, CW half-plane columns): G load, correction, column IFFT,
-//       store to the ring slot in 4-row tiles Z[slot][plane][ry/4][nx][ry%4];
+//       store to the ring slot, one column contiguous, Z[slot][plane][nx][ry]; the task
+//       that completes a plane's column pass also transforms its Nyquist-row term;
 //   row task (batch b, RT rows): for each plane of the batch, rebuild the full rows,
 //       row IFFT, phi = atan2, accumulate; then add the batch's per-pixel sums into the
 //       float64 S1 (and S2, object) in batch order.
-// A task waits only for tasks holding smaller tickets, so the schedule cannot deadlock
-// whatever the number of resident blocks.  Every wait is bounded; on timeout the kernel
-// raises an error flag, all waits stop and the host reports SSB_ERR_TIMEOUT.
+// A block takes its next ticket when its current task has finished its work: a column
+// task just before its completion fence (the round trips overlap), a row task after its
+// signal.  (Taking a column ticket any earlier, even just before the task's ring writes,
+// measured about 14 % slower overall.)  A task waits only for tasks holding smaller
+// tickets, so the schedule cannot deadlock whatever the number of resident blocks.
+// Every wait is bounded; on timeout the kernel raises an error flag, all waits stop and
+// the host reports SSB_ERR_TIMEOUT.
 #include <algorithm>
 
 #include "ssb_device.cuh"
@@ -39,6 +44,10 @@ namespace ssb {
 constexpr int kFusedThreads = SSB_FUSED_THREADS;  // threads per block (4 or 8 warps)
 constexpr int kFusedBlocksPerSM = 512 / kFusedThreads;
 constexpr int kPts = 16;                    // points per thread in every transform
+#ifndef SSB_COLS_PER_WARP
+#define SSB_COLS_PER_WARP 2
+#endif
+constexpr int kColsPerWarp = SSB_COLS_PER_WARP;  // half-plane columns per warp-group in a task
 constexpr unsigned kWaitLimit = 1u << 24;  // polls of ~0.1-1 us each before giving up
 
 struct FusedParams {
@@ -66,7 +75,7 @@ struct FusedShape {
     static constexpr int GROUPS = kFusedThreads / T;  // transforms per block
     static constexpr int H = N / 2 + 1;             // half-plane columns
     static constexpr int M = N / 2;                 // row transforms: M-point complex IFFT
-    static constexpr int CW = GROUPS;               // columns per column task
+    static constexpr int CW = GROUPS * kColsPerWarp;  // columns per column task
     static constexpr int RT = GROUPS < N ? GROUPS : N;  // rows per row task (multiple of 4)
     static constexpr int CT = (H + CW - 1) / CW;    // column tasks per plane
     static constexpr int NR = N / RT;               // row tasks per trial
@@ -78,8 +87,8 @@ struct FusedShape {
     // the column task's FFT scratch and the row task's scratch + staged planes share OFF_U.
     static constexpr int SMR = RegFFT<M, 8>::SMEM;                  // row FFT scratch per group
     static constexpr int OFF_TW = 0;                                // padded twiddles
-    static constexpr int OFF_TW2 = OFF_TW + (N + N / 8 + 2 + 1) / 2 * 2;  // M-point table
-    static constexpr int OFF_RED = OFF_TW2 + (M + M / 8 + 2 + 1) / 2 * 2;  // warp partials
+    static constexpr int OFF_TW2 = OFF_TW + (PadLen<N>::value + 1) / 2 * 2;  // M-point table
+    static constexpr int OFF_RED = OFF_TW2 + (PadLen<M>::value + 1) / 2 * 2;  // warp partials
     static constexpr int OFF_U = OFF_RED + 16;
     static constexpr int OFF_FFT = OFF_U;                           // column task: [GROUPS][SMF]
     static constexpr int OFF_RFFT = OFF_U;                          // row task: [GROUPS][SMR]
@@ -109,8 +118,18 @@ __device__ __forceinline__ void red_relaxed_add(unsigned *p, unsigned v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// Release by one thread after a block barrier: the block's earlier writes become visible
+// to any thread that observes the following relaxed write or reduction with an acquire.
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned *p, unsigned v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Called by one thread: wait until *addr >= target.  Returns false if the wait gave up
@@ -150,7 +169,7 @@ __device__ void nyquist_transform(const FusedParams &p, float2 *fsm, const float
         const float2 hm = (m >= 1) ? __ldcg(h + m) : make_float2(0.f, 0.f);
         const float2 hc = (mc >= 1 && mc < S::M) ? __ldcg(h + mc) : make_float2(0.f, 0.f);
         const float2 a = make_float2(hm.x + hc.x, hm.y - hc.y);
-        const float2 bb = cmul(make_float2(hm.x - hc.x, hm.y + hc.y), twid<+1>(twN, padx(m)));
+        const float2 bb = cmul(make_float2(hm.x - hc.x, hm.y + hc.y), twid<+1>(twN, lay(m)));
         v[r] = make_float2(a.x - bb.y, a.y + bb.x);
     }
     reg_fft<S::M, 8, +1>(v, fsm, twM, j, warp_bar);
@@ -161,80 +180,83 @@ __device__ void nyquist_transform(const FusedParams &p, float2 *fsm, const float
     }
 }
 
+// One column task.  free_word (NULL on the slot's first use) counts the row tasks of batch
+// b - D that have released this plane of the ring slot; the task overwrites the plane only
+// once all of them have.  Each warp reads the count when the task starts and checks it
+// before its first ring write, so the load's latency hides behind the column work.
+// Returns, uniform over the warp, whether the warp could write the slot.
 template <int N>
-__device__ void column_task(const FusedParams &p, float2 *smem, int b, int idx, unsigned *h_cnt,
-                            unsigned *err, int *s_ok) {
+__device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
+                           const unsigned *free_word, unsigned *err) {
     using S = FusedShape<N>;
-    const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
+    const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T, lane = tid & 31;
     const int kk = idx / S::CT, ct = idx - kk * S::CT;
     const int k = b * p.Bk + kk;
     const int slot = b % p.D;
-    const int nx = ct * S::CW + grp;
-    const bool valid = nx < S::H;
+    unsigned freed = (unsigned)S::NR;
+    if (lane == 0 && free_word) freed = ld_acquire(free_word);
     const float4 geo = __ldg(p.kgeo + k);
     const uint2 bt = __ldg(p.kturn + k);
-    float2 v[kPts];
-    if (valid) {
-        const float2 *g = p.G + ((size_t)k * S::H + nx) * N + j;
-        const float2 *e = p.Et + (size_t)nx * N + j;
-        float2 ev[kPts];
+    int ok = 1;
+#pragma unroll 1
+    for (int c = 0; c < kColsPerWarp; ++c) {
+        const int nx = ct * S::CW + c * S::GROUPS + grp;
+        const bool valid = nx < S::H;
+        float2 v[kPts];
+        float2 hval = make_float2(0.f, 0.f);
+        bool hstore = false;
+        if (valid) {
+            const float2 *g = p.G + ((size_t)k * S::H + nx) * N + j;
+            const float2 *e = p.Et + (size_t)nx * N + j;
+            float2 ev[kPts];
 #pragma unroll
-        for (int r = 0; r < kPts; ++r) {
-            v[r] = __ldcs(g + S::T * r);
-            ev[r] = __ldg(e + S::T * r);
-        }
-        const int sx = nx < N / 2 ? nx : nx - N;
-        const float lx0 = p.tc.lxs * (float)sx, ly0 = p.tc.lys * (float)sx;
-        const uint32_t phx = bt.x * (uint32_t)sx;
-        const bool active = geo.z > 0.0f;  // a(alpha_k) = 0: only the DC term survives
-#pragma unroll
-        for (int r = 0; r < kPts; ++r) {
-            const int ny = j + S::T * r;
-            const int sy = ny < N / 2 ? ny : ny - N;
-            const float2 gv = v[r];
-            float2 c = active ? correct_ssb2(gv, sy, ev[r], geo.x, geo.y, phx, bt.y, lx0, ly0, p.tc)
-                              : make_float2(0.f, 0.f);
-            if ((nx | ny) == 0) c = gv;  // C(0) = G(0)
-            if (r == kPts / 2 && j == 0 && nx >= 1 && nx < N / 2) {
-                // Nyquist row (ny = N/2): the mirror bin N - nx has no partner and carries
-                // its own correction, at signed bins (-nx, -N/2)
-                const float2 em = __ldg(p.Et + (size_t)(N - nx) * N + N / 2);
-                const float2 c2 = active ? correct_ssb2(cconj(gv), -N / 2, em, geo.x, geo.y,
-                                                        0u - phx, bt.y, -lx0, -ly0, p.tc)
-                                         : make_float2(0.f, 0.f);
-                const float2 h = make_float2(0.5f * (c.x + c2.x), 0.5f * (c.y - c2.y));
-                __stcg(p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ + nx, h);
+            for (int r = 0; r < kPts; ++r) {
+                v[r] = __ldcs(g + S::T * r);
+                ev[r] = __ldg(e + S::T * r);
             }
-            v[r] = c;
+            const int sx = nx < N / 2 ? nx : nx - N;
+            const float lx0 = p.tc.lxs * (float)sx, ly0 = p.tc.lys * (float)sx;
+            const uint32_t phx = bt.x * (uint32_t)sx;
+            const bool active = geo.z > 0.0f;  // a(alpha_k) = 0: only the DC term survives
+#pragma unroll
+            for (int r = 0; r < kPts; ++r) {
+                const int ny = j + S::T * r;
+                const int sy = ny < N / 2 ? ny : ny - N;
+                const float2 gv = v[r];
+                float2 cv = active ? correct_ssb2(gv, sy, ev[r], geo.x, geo.y, phx, bt.y, lx0, ly0, p.tc)
+                                   : make_float2(0.f, 0.f);
+                if ((nx | ny) == 0) cv = gv;  // C(0) = G(0)
+                if (r == kPts / 2 && j == 0 && nx >= 1 && nx < N / 2) {
+                    // Nyquist row (ny = N/2): the mirror bin N - nx has no partner and
+                    // carries its own correction, at signed bins (-nx, -N/2)
+                    const float2 em = __ldg(p.Et + (size_t)(N - nx) * N + N / 2);
+                    const float2 c2 = active ? correct_ssb2(cconj(gv), -N / 2, em, geo.x, geo.y,
+                                                            0u - phx, bt.y, -lx0, -ly0, p.tc)
+                                             : make_float2(0.f, 0.f);
+                    hval = make_float2(0.5f * (cv.x + c2.x), 0.5f * (cv.y - c2.y));
+                    hstore = true;
+                }
+                v[r] = cv;
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < kPts; ++r) v[r] = make_float2(0.f, 0.f);
         }
-    } else {
+        reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
+        if (c == 0) {
+            if (lane == 0 && freed < (unsigned)S::NR)
+                ok = wait_at_least(free_word, (unsigned)S::NR, err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();  // the warp's ring writes follow lane 0's acquire
+        }
+        if (valid && ok) {
+            float2 *z = p.Z + (((size_t)slot * p.Bk + kk) * S::H + nx) * N + j;
 #pragma unroll
-        for (int r = 0; r < kPts; ++r) v[r] = make_float2(0.f, 0.f);
+            for (int r = 0; r < kPts; ++r) __stcg(z + S::T * r, v[r]);
+            if (hstore) __stcg(p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ + nx, hval);
+        }
     }
-    reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
-    if (valid) {
-        float2 *z = p.Z + (((size_t)slot * p.Bk + kk) * S::H + nx) * N + j;
-#pragma unroll
-        for (int r = 0; r < kPts; ++r) __stcg(z + S::T * r, v[r]);
-    }
-    // Once every column task of the plane has written its Nyquist terms, the plane's last
-    // column task transforms them with its last warp, whose groups are all idle there (the
-    // last task holds at most one warp's worth of valid columns for every supported N).
-    __syncthreads();
-    unsigned *hc = h_cnt + (size_t)b * p.Bk + kk;
-    if (tid == 0) {
-        __threadfence();  // publishes this task's ring columns and h values
-        atomicAdd(hc, 1u);
-    }
-    if (ct == S::CT - 1) {
-        if (tid == 0) *s_ok = wait_at_least(hc, (unsigned)S::CT, err);
-        __syncthreads();
-        static_assert(S::H - (S::CT - 1) * S::CW <= S::CW - 32 / S::T,
-                      "the last column task must leave its last warp idle");
-        if (tid >= kFusedThreads - 32 && *s_ok)  // whole warp: the transform syncs the warp
-            nyquist_transform<N>(p, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW,
-                                 smem + S::OFF_TW2, slot, kk, j, grp == S::GROUPS - 1);
-    }
+    return ok;
 }
 
 // ---------------------------------------------------------------- row task
@@ -268,7 +290,7 @@ __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk
 //   Re c = Re Z(0) + (-1)^rx Re Z(N/2) + s Rp(rx),   s = (-1)^ry.
 template <int N, bool OBJ>
 __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int planes,
-                         unsigned *plane_free, unsigned *chain, unsigned *err, int *s_ok) {
+                             unsigned *plane_free, unsigned *chain, unsigned *err, int *s_ok) {
     using S = FusedShape<N>;
     const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
     const int slot = b % p.D;
@@ -323,7 +345,7 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
                 yc = make_float2(fmaf(-sg, hb.y, zb.y), fmaf(sg, hb.x, -zb.x));
             }
             const float2 a = make_float2(ym.x + yc.x, ym.y - yc.y);
-            const float2 bb = cmul(make_float2(ym.x - yc.x, ym.y + yc.y), twid<+1>(twN, padx(m)));
+            const float2 bb = cmul(make_float2(ym.x - yc.x, ym.y + yc.y), twid<+1>(twN, lay(m)));
             v[r] = active ? make_float2(a.x - bb.y, a.y + bb.x) : make_float2(0.f, 0.f);
         }
         reg_fft<S::M, 8, +1>(v, smem + S::OFF_RFFT + grp * S::SMR, smem + S::OFF_TW2, j, warp_bar);
@@ -349,16 +371,30 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
     if (tid == 0) *s_ok = wait_at_least(chain + rt, (unsigned)b, err);
     __syncthreads();
     if (active && *s_ok) {
+        // Loads are issued in groups ahead of their stores: a store through the same
+        // pointer would otherwise hold back each following load for a full round trip.
+        // A thread owns pixel pairs (2 (j + T r), 2 (j + T r) + 1).  With the object sums
+        // live, smaller groups keep the registers within the launch bound.
+        constexpr int GS = OBJ ? 2 : 8;  // S1 pixel pairs per group
+        double2 *s1 = reinterpret_cast<double2 *>(p.S1 + (size_t)ry * N) + j;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int g0 = 0; g0 < 8; g0 += GS) {
+            double2 old[GS];
 #pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-                const size_t i = (size_t)ry * N + 2 * (j + S::T * r) + e2;
-                p.S1[i] = __ldcg(p.S1 + i) + (double)acc1[2 * r + e2];
-                if (OBJ) {
-                    const double2 o = __ldcg(p.Osum + i);
-                    p.Osum[i] = make_double2(o.x + acco[2 * r + e2].x, o.y + acco[2 * r + e2].y);
-                }
+            for (int r = 0; r < GS; ++r) old[r] = __ldcg(s1 + S::T * (g0 + r));
+#pragma unroll
+            for (int r = 0; r < GS; ++r)
+                s1[S::T * (g0 + r)] = make_double2(old[r].x + (double)acc1[2 * (g0 + r)],
+                                                   old[r].y + (double)acc1[2 * (g0 + r) + 1]);
+        }
+        if (OBJ) {
+            double2 *os = p.Osum + (size_t)ry * N + 2 * j;  // pixel 2 (j + T r) + e at 2 T r + e
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const double2 o0 = __ldcg(os + 2 * S::T * r), o1 = __ldcg(os + 2 * S::T * r + 1);
+                const float2 a0 = acco[2 * r], a1 = acco[2 * r + 1];
+                os[2 * S::T * r] = make_double2(o0.x + a0.x, o0.y + a0.y);
+                os[2 * S::T * r + 1] = make_double2(o1.x + a1.x, o1.y + a1.y);
             }
         }
     }
@@ -423,9 +459,10 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(Fuse
     extern __shared__ __align__(16) float2 smem[];
     __shared__ unsigned s_ticket;
     __shared__ int s_ok;
+    __shared__ int s_nyq;
     const int tid = threadIdx.x;
-    for (int i = tid; i < N; i += kFusedThreads) smem[S::OFF_TW + padx(i)] = p.tw[i];
-    for (int i = tid; i < S::M; i += kFusedThreads) smem[S::OFF_TW2 + padx(i)] = p.tw[2 * i];
+    for (int i = tid; i < N; i += kFusedThreads) smem[S::OFF_TW + lay(i)] = p.tw[i];
+    for (int i = tid; i < S::M; i += kFusedThreads) smem[S::OFF_TW2 + lay(i)] = p.tw[2 * i];
     unsigned *ticket = p.sync;
     unsigned *err = p.sync + 1;
     unsigned *col_done = p.sync + 2;
@@ -433,31 +470,47 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(Fuse
     unsigned *h_cnt = plane_free + (size_t)p.nbatch * p.Bk;
     unsigned *chain = h_cnt + (size_t)p.nbatch * p.Bk;
     __syncthreads();
+    // The ticket in s_ticket is read after the barrier at the top of the loop; thread 0
+    // takes the next one only after the task's last barrier and its completion signals.
+    if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
     while (true) {
-        if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
         __syncthreads();
         const Task task = decode_ticket<N>(p, s_ticket);
         if (task.kind == 2) break;
-        if (tid == 0) {
-            bool ok = true;
-            if (task.kind == 0) {
-                if (task.b >= p.D)  // this plane of the ring slot is read by rows of b - D
-                    ok = wait_at_least(plane_free + (size_t)(task.b - p.D) * p.Bk + task.idx / S::CT,
-                                       (unsigned)S::NR, err);
-            } else {
-                ok = wait_at_least(col_done + task.b, (unsigned)(planes_in(p, task.b) * S::CT), err);
-            }
-            s_ok = ok;
-        }
-        __syncthreads();
         if (task.kind == 0) {
-            if (s_ok) column_task<N>(p, smem, task.b, task.idx, h_cnt, err, &s_ok);
+            const int kk = task.idx / S::CT;
+            // this plane of the ring slot was last read by the row tasks of batch b - D
+            const unsigned *free_word =
+                task.b >= p.D ? plane_free + (size_t)(task.b - p.D) * p.Bk + kk : nullptr;
+            const int ok = column_task<N>(p, smem, task.b, task.idx, free_word, err);
             __syncthreads();
             if (tid == 0) {
-                __threadfence();
-                atomicAdd(col_done + task.b, 1u);
+                // the next ticket's round trip overlaps the fence
+                const unsigned next = atomicAdd(ticket, 1u);
+                fence_acq_rel();  // publishes the task's ring columns and Nyquist terms
+                // The task that completes the plane's column pass also transforms the
+                // plane's Nyquist terms (it acquires the others' h with the count).
+                const unsigned done = atom_add_acq_rel(h_cnt + (size_t)task.b * p.Bk + kk, 1u) + 1u;
+                s_nyq = done == (unsigned)S::CT;
+                if (!s_nyq) red_relaxed_add(col_done + task.b, 1u);
+                s_ticket = next;
+            }
+            __syncthreads();
+            if (s_nyq) {
+                if (tid < 32 && ok)  // whole warp: the transform synchronises the warp
+                    nyquist_transform<N>(p, smem + S::OFF_FFT + (tid / S::T) * S::SMF,
+                                         smem + S::OFF_TW, smem + S::OFF_TW2, task.b % p.D, kk,
+                                         tid % S::T, tid < S::T);
+                __syncthreads();
+                if (tid == 0) {
+                    fence_acq_rel();  // publishes Rp
+                    red_relaxed_add(col_done + task.b, 1u);
+                }
             }
         } else {
+            if (tid == 0)
+                s_ok = wait_at_least(col_done + task.b, (unsigned)(planes_in(p, task.b) * S::CT), err);
+            __syncthreads();
             if (s_ok) {
                 row_task<N, OBJ>(p, smem, task.b, task.idx, planes_in(p, task.b), plane_free,
                                  chain, err, &s_ok);
@@ -467,8 +520,9 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(Fuse
             }
             __syncthreads();
             if (tid == 0) {
-                __threadfence();
-                st_release(chain + task.idx, (unsigned)task.b + 1u);
+                fence_acq_rel();  // publishes the task's S1, S2 (and object) updates
+                st_relaxed(chain + task.idx, (unsigned)task.b + 1u);
+                s_ticket = atomicAdd(ticket, 1u);
             }
         }
     }

@@ -5,7 +5,7 @@
 // Thread j of the group holds x[j + T r] (r = 0..E-1) on entry and X[j + T r] on exit
 // (natural order on both sides).  Passes follow Stockham's self-sorting schedule (radix 8,
 // then a final radix 4 or 2 when log2 N is not a multiple of 3); between passes the
-// points go through a padded shared-memory buffer of N + N/8 complex values per group.
+// points go through a shared-memory buffer of PadLen<N> complex values per group.
 // A radix-R pass has N/R butterflies: butterfly b reads x[b + (N/R) q], twists it by
 // exp(S 2 pi i q (b mod Ns) / (Ns R)), takes the R-point DFT and writes
 // y[(b - b mod Ns) R + b mod Ns + Ns q].  Thread j runs butterflies b = j + T m,
@@ -17,14 +17,31 @@
 
 namespace ssb {
 
-// Padded shared-memory index: one spare slot every 8 complex values keeps the pass
-// exchanges (and twiddle reads) free of most bank conflicts for 64-bit accesses.
-__device__ __forceinline__ int padx(int i) { return i + (i >> 3); }
+// Padded shared-memory slot of complex value i: one spare slot every 16.  For 64-bit
+// accesses (16 lanes per 128-byte wavefront) this keeps the exchange reads, the first
+// pass's writes and the twiddle reads free of bank conflicts; the second pass's writes
+// (span 8) take two-way conflicts.  Among paddings i + sum c_s (i >> s) none does better
+// for the 512- and 256-point transforms, and a padding keeps every access of a pass at a
+// constant offset from one per-thread base.  (An XOR swizzle that removes the remaining
+// conflicts too measured no faster: its offsets cost instructions.)
+constexpr int kPadShift = 4;
+__device__ __forceinline__ int lay(int i) { return i + (i >> kPadShift); }
+template <int N>
+struct PadLen {
+    static constexpr int value = N + (N >> kPadShift);
+};
+// lay(j + T r) from base = lay(j), for j < T and T a multiple of 16
+template <int T>
+__device__ __forceinline__ int lay_seq(int base, int r) { return base + lay(T * r); }
+// lay(o + Ns q) from base = lay(o): o a multiple of 8 when Ns = 1, o mod 16 < 8 when Ns = 8
+__device__ __forceinline__ int lay_out(int base, int Ns, int q) { return base + lay(Ns * q); }
+// lay(i + c) = lay(i) + lay_shift(c) for c a multiple of 16
+__device__ __forceinline__ int lay_shift(int c) { return lay(c); }
 
 template <int N, int E>
 struct RegFFT {
     static constexpr int T = N / E;
-    static constexpr int SMEM = N + N / 8;  // complex values per group
+    static constexpr int SMEM = PadLen<N>::value;  // complex values per group
     static constexpr int LOG2N = N == 16 ? 4 : N == 32 ? 5 : N == 64 ? 6 : N == 128 ? 7 : N == 256 ? 8 : 9;
     static constexpr int N8 = LOG2N / 3;        // radix-8 passes
     static constexpr int TAIL = LOG2N - 3 * N8; // 0, 1 (radix 2) or 2 (radix 4)
@@ -51,12 +68,19 @@ __device__ __forceinline__ void dft8(float2 (&v)[8]) {
 }
 
 // One Stockham pass of radix R (8, 4 or 2) over the group's registers, span Ns.
-// twp is the padded twiddle table: twp[padx(m)] = exp(+2 pi i m / N).
+// twp is the twiddle table in the same layout: twp[lay(m)] = exp(+2 pi i m / N).
+// Non-final passes are radix 8 with Ns = 1 or 8; with T a multiple of 16 every slot a
+// thread touches is a constant offset from one per-thread base (lay_seq, lay_out and
+// lay_shift), otherwise each slot is computed in full.
 template <int N, int E, int R, int S, bool LAST, typename Bar>
 __device__ __forceinline__ void stockham_pass(float2 (&v)[E], float2 *sm, const float2 *twp,
                                               int j, int Ns, Bar bar) {
     constexpr int T = N / E;
     constexpr int PER = E / R;  // butterflies per thread
+    constexpr bool kSeq = T % 16 == 0;
+    // outputs of butterfly m start at (b - k) R + k = o0 + R T m (k = j mod Ns for Ns <= T)
+    const int k0 = j & (Ns - 1);
+    const int wbase = lay((j - k0) * R + k0);
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
         const int b = j + T * m;
@@ -66,7 +90,7 @@ __device__ __forceinline__ void stockham_pass(float2 (&v)[E], float2 *sm, const 
         for (int q = 0; q < R; ++q) u[q] = v[m + PER * q];
         if (Ns > 1) {
             // one table read, the other twiddles as products of it (depth 3 for radix 8)
-            const float2 w1 = twid<S>(twp, padx(k * (N / (Ns * R))));
+            const float2 w1 = twid<S>(twp, lay(k * (N / (Ns * R))));
             if (R == 2) {
                 u[1] = cmul(u[1], w1);
             } else {
@@ -106,15 +130,19 @@ __device__ __forceinline__ void stockham_pass(float2 (&v)[E], float2 *sm, const 
 #pragma unroll
             for (int q = 0; q < R; ++q) v[m + PER * q] = u[q];
         } else {
-            const int o = (b - k) * R + k;
 #pragma unroll
-            for (int q = 0; q < R; ++q) sm[padx(o + Ns * q)] = u[q];
+            for (int q = 0; q < R; ++q) {
+                const int a = kSeq ? lay_out(wbase, Ns, q) + lay_shift(R * T * m)
+                                   : lay((b - k) * R + k + Ns * q);
+                sm[a] = u[q];
+            }
         }
     }
     if (!LAST) {
         bar();
+        const int rbase = lay(j);
 #pragma unroll
-        for (int r = 0; r < E; ++r) v[r] = sm[padx(j + T * r)];
+        for (int r = 0; r < E; ++r) v[r] = sm[kSeq ? lay_seq<T>(rbase, r) : lay(j + T * r)];
         bar();
     }
 }
