@@ -105,7 +105,21 @@ struct TrialConst {
     float lxs, lxy, lys, lyy;
     float inner2;       // |alpha|^2 at or below which a(alpha) = 1 (negative: never)
     float outer2;       // |alpha|^2 at or above which a(alpha) = 0
+    float lam_q;        // lambda / (N * scan step): |lambda Q'| per frequency bin (rad)
+    float zero_r;       // outer aperture radius with a 1e-4 margin (rad), see column_zero
 };
+
+// True when both shifted apertures vanish on the whole scan-frequency column sx of BF
+// pixel alpha_k = (ax, ay), so that the column's SSB2 transfer is exactly zero.  As sy
+// runs, lambda Q'(sx, sy) traces the line sx lam_q (cos, sin) + t (-sin, cos); its
+// distance from alpha_k is |u - sx lam_q| and from -alpha_k |u + sx lam_q|, with
+// u = ax cos + ay sin.  Both distances at least zero_r (the outer radius plus a 1e-4
+// margin, far above float32 rounding) put every element outside both apertures.
+__device__ __forceinline__ bool column_zero(int sx, float ax, float ay, const TrialConst &tc) {
+    const float u = fmaf(ax, tc.cr, ay * tc.sr);
+    const float o = tc.lam_q * (float)sx;
+    return fabsf(u - o) >= tc.zero_r && fabsf(u + o) >= tc.zero_r;
+}
 
 // Amplitudes below this are exactly zero transfer: a scan grid commensurate with the
 // detector can put a shifted aperture exactly on its outer edge, where the unit-modulus

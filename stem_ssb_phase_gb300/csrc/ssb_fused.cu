@@ -202,10 +202,16 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
     for (int c = 0; c < kColsPerWarp; ++c) {
         const int nx = ct * S::CW + c * S::GROUPS + grp;
         const bool valid = nx < S::H;
+        const int sx = nx < N / 2 ? nx : nx - N;
+        // Columns with exactly zero transfer (both shifted apertures miss the whole column;
+        // every column but DC for an inactive BF pixel) skip the loads, the correction and
+        // the transform and store zeros.  The decision is uniform over the warp.
+        const bool zero = nx > 0 && (!(geo.z > 0.0f) || column_zero(sx, geo.x, geo.y, p.tc));
+        const bool skip = __all_sync(0xffffffffu, zero || !valid);
         float2 v[kPts];
         float2 hval = make_float2(0.f, 0.f);
-        bool hstore = false;
-        if (valid) {
+        bool hstore = skip && j == 0 && nx >= 1 && nx < N / 2;  // h = 0 there
+        if (valid && !skip) {
             const float2 *g = p.G + ((size_t)k * S::H + nx) * N + j;
             const float2 *e = p.Et + (size_t)nx * N + j;
             float2 ev[kPts];
@@ -214,7 +220,6 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
                 v[r] = __ldcs(g + S::T * r);
                 ev[r] = __ldg(e + S::T * r);
             }
-            const int sx = nx < N / 2 ? nx : nx - N;
             const float lx0 = p.tc.lxs * (float)sx, ly0 = p.tc.lys * (float)sx;
             const uint32_t phx = bt.x * (uint32_t)sx;
             const bool active = geo.z > 0.0f;  // a(alpha_k) = 0: only the DC term survives
@@ -242,7 +247,8 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
 #pragma unroll
             for (int r = 0; r < kPts; ++r) v[r] = make_float2(0.f, 0.f);
         }
-        reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
+        if (!skip)
+            reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
         if (c == 0) {
             if (lane == 0 && freed < (unsigned)S::NR)
                 ok = wait_at_least(free_word, (unsigned)S::NR, err);

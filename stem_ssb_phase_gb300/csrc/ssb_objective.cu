@@ -211,6 +211,8 @@ TrialConst make_trial_const(const ObjectiveArgs &a, const TrialHost &th, int N) 
     const double inner = a.semi - 0.5 * a.dalpha, outer = a.semi + 0.5 * a.dalpha;
     tc.inner2 = inner > 0.0 ? (float)(inner * inner) * (1.0f - 4e-7f) : -1.0f;
     tc.outer2 = (float)(outer * outer) * (1.0f + 4e-7f);
+    tc.lam_q = (float)q;
+    tc.zero_r = (float)(outer * (1.0 + 1e-4));
     return tc;
 }
 
