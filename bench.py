@@ -115,12 +115,9 @@ class ClockSampler:
 def _algorithmic_bytes(n_bf: int, n: int) -> dict:
     """Bytes each kernel must move per objective, by kernel name: the G cache read once
     (n_bf x (N/2+1) x N complex64).  The fused kernel keeps the column-pass intermediate in
-    L2, so the G read is all it must move; the two-kernel SSB1 path also writes and reads
-    the full-plane intermediate once."""
+    L2, so the G read is all it must move (for either transfer)."""
     h = n // 2 + 1
-    g = n_bf * h * n * 8
-    x = n_bf * n * n * 8
-    return {"k_fused": g, "k_correct_cols": g + x, "k_rows_moments": x}
+    return {"k_fused": n_bf * h * n * 8}
 
 
 def _traffic_record():
@@ -160,10 +157,10 @@ def job_throughput(world: int, steps: int, units_per_step: float, seconds: float
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
-def cpu_oracle_run(geom, counts_sample, theta, workers: int):
+def cpu_oracle_run(geom, counts_sample, theta, workers: int, mode: str = "ssb2"):
     import oracle
     t0 = time.perf_counter()
-    res = oracle.objective(geom, theta, counts=counts_sample, workers=workers,
+    res = oracle.objective(geom, theta, counts=counts_sample, workers=workers, mode=mode,
                            bf_range=(0, counts_sample.shape[0]))
     return time.perf_counter() - t0, res["loss"]
 
@@ -198,7 +195,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = counts[: min(geom.n_bf, 16 * cores * 4)].cpu().numpy()
         sample = sample.view(np.uint32) if w.dtype == "u32" else sample.view(np.uint16)
-    ctx = ssbgpu.SSB(geom, counts)
+    ctx = ssbgpu.SSB(geom, counts, transfer=args.transfer)
     del counts
     torch.cuda.empty_cache()
     thetas = ssb_synth.draw_trials(w, args.trials)
@@ -282,9 +279,9 @@ def run_ours(args, rank, world, local_rank):
     cpu = None
     if sample is not None:
         import oracle
-        per_bf, _ = cpu_oracle_run(geom, sample[:1], thetas[0], workers=1)
+        per_bf, _ = cpu_oracle_run(geom, sample[:1], thetas[0], workers=1, mode=args.transfer)
         s = min(sample.shape[0], cpu_sample_size(geom.n_bf, cores, per_bf))
-        t_cpu, _ = cpu_oracle_run(geom, sample[:s], thetas[0], workers=cores)
+        t_cpu, _ = cpu_oracle_run(geom, sample[:s], thetas[0], workers=cores, mode=args.transfer)
         cpu = {"value": s * n * n / t_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "%d of %d BF pixels of the same workload, one trial, float64 NumPy "
                          "oracle in %d spawned processes (%.1f s)" % (s, geom.n_bf, cores, t_cpu)}
@@ -300,7 +297,7 @@ def run_ours(args, rank, world, local_rank):
                                    "complex64 Hermitian G cache %.2f GB" % (
                                        w.name, n, n, w.det_n, w.det_n, geom.n_bf, w.dtype,
                                        w.mean_count, objective_bytes / 1e9),
-                       "trials_per_step": args.trials, "transfer": "ssb2",
+                       "trials_per_step": args.trials, "transfer": args.transfer,
                        "l2": "inputs (G cache %.1f GB) exceed the 129 MB L2; no flush" % (objective_bytes / 1e9),
                        "parallelism": "replicas x%d" % world},
             "e2e": e2e,
@@ -385,10 +382,10 @@ def run_reference(args, rank, world):
     _, counts, _ = ssb_synth.simulate_counts_numpy(w, geom=geom)
     theta = ssb_synth.draw_trials(w, 1)[0]
     for _ in range(args.warmup):
-        cpu_oracle_run(geom, counts, theta, workers=cores)
+        cpu_oracle_run(geom, counts, theta, workers=cores, mode=args.transfer)
     times = []
     for _ in range(args.steps):
-        t, loss = cpu_oracle_run(geom, counts, theta, workers=cores)
+        t, loss = cpu_oracle_run(geom, counts, theta, workers=cores, mode=args.transfer)
         times.append(t)
     tot = sum(times)
     value = args.steps * s * n * n / tot
@@ -399,7 +396,8 @@ def run_reference(args, rank, world):
            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": value / (2342780928 / (PAGES_MS / 1e3)) if args.workload == "full" else None,
            "dtype": "f64", "data": "synthetic",
-           "config": {"workload": "%s (BF sample)" % w.name, "bf_sample": s, "trials_per_step": 1},
+           "config": {"workload": "%s (BF sample)" % w.name, "bf_sample": s, "trials_per_step": 1,
+                      "transfer": args.transfer},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -414,6 +412,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--trials", type=int, default=1)
+    ap.add_argument("--transfer", choices=["ssb2", "ssb1"], default="ssb2",
+                    help="ssb2: normalised two-sideband transfer (default); ssb1: the literal "
+                         "single-sideband factor exp(i(chi(q_k) - chi(q_k - Q))) with the mask")
     ap.add_argument("--workload", default="full", choices=sorted(ssb_synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fit", action="store_true",

@@ -92,7 +92,7 @@ using namespace ssb;
 
 struct ssb_ctx {
     int dev = 0;
-    int N = 0, n_bf = 0, B = 0;
+    int N = 0, n_bf = 0;
     double step = 0, lam = 0, semi = 0, dalpha = 0;
     ssb_transfer transfer = SSB_TRANSFER_SSB2;
     float2 *G = nullptr;
@@ -101,8 +101,7 @@ struct ssb_ctx {
     uint2 *kturn = nullptr;
     float2 *E = nullptr;
     float2 *tw = nullptr;
-    float2 *X = nullptr;
-    double *S1 = nullptr, *S2 = nullptr;
+    double *S1 = nullptr;
     double2 *Osum = nullptr;
     double *loss = nullptr;
     int loss_cap = 0;
@@ -110,7 +109,6 @@ struct ssb_ctx {
     double *S2g = nullptr;
     unsigned *sync = nullptr;
     int Bk = 0, D = 0;
-    bool fused = false;
     int *flag = nullptr;
     size_t g_bytes = 0, scratch_bytes = 0;
 
@@ -124,10 +122,7 @@ struct ssb_ctx {
         a.kturn = kturn;
         a.E = E;
         a.tw = tw;
-        a.X = X;
-        a.B = B;
         a.S1 = S1;
-        a.S2 = S2;
         a.Osum = Osum;
         a.loss = loss;
         a.Zring = Zring;
@@ -148,8 +143,8 @@ struct ssb_ctx {
 
 static void free_ctx(ssb_ctx *c) {
     if (!c) return;
-    void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->X, c->S1, c->S2,
-                    c->Osum, c->loss, c->flag, c->Zring, c->hring, c->rring, c->S2g, c->sync};
+    void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->S1, c->Osum,
+                    c->loss, c->flag, c->Zring, c->hring, c->rring, c->S2g, c->sync};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete c;
@@ -159,13 +154,11 @@ static bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
 
 static cudaError_t evaluate(const ssb_ctx *c, const ssb_params &theta, double *loss_slot,
                             bool want_object, cudaStream_t s) {
-    return c->fused ? run_objective_fused(c->args(), theta, loss_slot, want_object, s)
-                    : run_objective(c->args(), theta, loss_slot, want_object, s);
+    return run_objective_fused(c->args(), theta, loss_slot, want_object, s);
 }
 
-// After a fused evaluation: the scheduler's error word (a bounded wait that ran out).
+// After an evaluation: the scheduler's error word (a bounded wait that ran out).
 static ssb_status check_sync(const ssb_ctx *c, cudaStream_t s) {
-    if (!c->fused) return SSB_OK;
     unsigned h = 0;
     SSB_CK(cudaMemcpyAsync(&h, c->sync + 1, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
     SSB_CK(cudaStreamSynchronize(s));
@@ -252,8 +245,6 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     c->transfer = transfer;
     const int H = N / 2 + 1;
     const size_t P = (size_t)N * N;
-    const size_t per_bf_x = P * sizeof(float2);
-    c->B = (int)std::max<size_t>(1, std::min<size_t>((size_t)c->n_bf, (64u << 20) / per_bf_x));
 
     ssb_status st = SSB_OK;
     auto bail = [&](ssb_status code) {
@@ -273,23 +264,18 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     SSB_ALLOC(c->kturn, (size_t)c->n_bf, sb);
     SSB_ALLOC(c->E, P, sb);
     SSB_ALLOC(c->tw, (size_t)N, sb);
-    // SSB2 runs on the persistent fused kernel; SSB1 on the batched two-kernel path
-    c->fused = transfer == SSB_TRANSFER_SSB2;
-    // batch size and ring depth of the fused path: several short batches in flight keep
-    // the column work flowing while slow row tasks drain the oldest slots, within an
-    // L2-sized ring (about 50 MB at N = 512)
-    c->Bk = std::min(SSB_FUSED_BK, c->n_bf);
+    // Both transfers run on the persistent fused kernel.  Batch size and ring depth:
+    // several short batches in flight keep the column work flowing while slow row tasks
+    // drain the oldest slots, within an L2-sized ring (about 67 MB at N = 512; SSB1
+    // transforms all N columns, so its batches hold half the planes)
+    const bool ssb1 = transfer == SSB_TRANSFER_SSB1;
+    c->Bk = std::min(ssb1 ? SSB_FUSED_BK / 2 : SSB_FUSED_BK, c->n_bf);
     c->D = SSB_FUSED_RING;
-    if (c->fused) {
-        SSB_ALLOC(c->Zring, fused_ring_elems(N, c->Bk, c->D), sb);
-        SSB_ALLOC(c->hring, fused_hring_elems(N, c->Bk, c->D), sb);
-        SSB_ALLOC(c->rring, fused_rring_elems(N, c->Bk, c->D), sb);
-        SSB_ALLOC(c->S2g, (size_t)fused_row_tasks(N), sb);
-        SSB_ALLOC(c->sync, fused_sync_words(N, c->n_bf, c->Bk), sb);
-    } else {
-        SSB_ALLOC(c->X, (size_t)c->B * P, sb);
-        SSB_ALLOC(c->S2, P, sb);
-    }
+    SSB_ALLOC(c->Zring, fused_ring_elems(N, c->Bk, c->D, ssb1), sb);
+    SSB_ALLOC(c->hring, fused_hring_elems(N, c->Bk, c->D), sb);
+    SSB_ALLOC(c->rring, fused_rring_elems(N, c->Bk, c->D), sb);
+    SSB_ALLOC(c->S2g, (size_t)fused_row_tasks(N), sb);
+    SSB_ALLOC(c->sync, fused_sync_words(N, c->n_bf, c->Bk), sb);
     SSB_ALLOC(c->S1, P, sb);
     SSB_ALLOC(c->Osum, P, sb);
     c->loss_cap = 4096;

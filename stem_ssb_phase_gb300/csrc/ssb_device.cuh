@@ -89,10 +89,6 @@ __device__ int fft_batch_smem(float2 *buf0, float2 *buf1, int NF, int LD, const 
     return which;
 }
 
-// fftfreq ordering: bins 0..N/2-1 are non-negative, N/2..N-1 negative (Nyquist negative).
-template <int N>
-__device__ __forceinline__ int signed_bin(int q) { return q < N / 2 ? q : q - N; }
-
 // Per-trial constants of the correction (float32 copies of host float64 values).
 struct TrialConst {
     float cr, sr;       // cos, sin of the scan rotation
@@ -120,19 +116,20 @@ __device__ __forceinline__ bool column_zero(int sx, float ax, float ay, const Tr
     const float o = tc.lam_q * (float)sx;
     return fabsf(u - o) >= tc.zero_r && fabsf(u + o) >= tc.zero_r;
 }
+// The SSB1 transfer needs only the aperture at alpha_k - lambda Q': the column is zero when
+// its line passes at least zero_r from alpha_k.
+__device__ __forceinline__ bool column_zero1(int sx, float ax, float ay, const TrialConst &tc) {
+    const float u = fmaf(ax, tc.cr, ay * tc.sr);
+    return fabsf(u - tc.lam_q * (float)sx) >= tc.zero_r;
+}
 
 // Amplitudes below this are exactly zero transfer: a scan grid commensurate with the
 // detector can put a shifted aperture exactly on its outer edge, where the unit-modulus
 // normalisation would otherwise let rounding choose between zero and a full-size term.
 constexpr float kApertureFloor = 1.0f / 65536.0f;
 
-__device__ __forceinline__ float soft_aperture(float ax, float ay, float semi, float inv_da) {
-    const float r = sqrtf(fmaf(ax, ax, ay * ay));
-    const float a = fminf(fmaxf(fmaf(semi - r, inv_da, 0.5f), 0.0f), 1.0f);
-    return a < kApertureFloor ? 0.0f : a;
-}
-
-// Soft aperture from |alpha|^2 with exact inside/outside shortcuts: a = 1 for
+// Soft aperture a(alpha) = clip((alpha_c - |alpha|)/d_alpha + 1/2, 0, 1), from |alpha|^2,
+// with exact inside/outside shortcuts: a = 1 for
 // |alpha| <= alpha_c - d_alpha/2 and a = 0 for |alpha| >= alpha_c + d_alpha/2 need no
 // square root; the rim between them takes the full expression and the zero floor.
 __device__ __forceinline__ float aperture_r2(float r2, const TrialConst &tc) {
@@ -143,9 +140,16 @@ __device__ __forceinline__ float aperture_r2(float r2, const TrialConst &tc) {
     return a < kApertureFloor ? 0.0f : a;
 }
 
-// SSB2 correction of one G value at signed bins (sx, sy), with the per-column terms
-// hoisted by the caller: lx0 = lxs sx, ly0 = lys sx, phx = b_x sx (turn fraction).
-// Same algebra as correction_factor below; DC and a_k = 0 are handled by the caller.
+// SSB2 correction of one G value at signed bins (sx, sy): C = G conj(Gamma)/|Gamma|, 0 where
+// Gamma = 0.  With chi quadratic, chi(alpha_k -+ lambda Q') = chi(alpha_k) + chi(lambda Q')
+// -+ B with B = 2 pi alpha_k^T M Q' linear in Q (M the aberration matrix), so
+//   Gamma_k = a_k e^{-iB} [a_- e^{i chiQ} - a_+ e^{-i chiQ}] = a_k e^{-iB} D,
+//   D = (a_- - a_+) cos chiQ + i (a_- + a_+) sin chiQ,
+// and conj(Gamma)/|Gamma| = e^{iB} conj(D)/|D| (an exact rewriting).  chiQ comes from the
+// per-trial table E = e^{i chiQ}; B is carried exactly as a 32-bit fixed-point fraction of
+// a turn, b_x sx + b_y sy mod 2^32, so its range reduction is exact.  The per-column terms
+// are hoisted by the caller: lx0 = lxs sx, ly0 = lys sx, phx = b_x sx; DC (C(0) = G(0))
+// and a_k = 0 are handled there too.
 __device__ __forceinline__ float2 correct_ssb2(float2 g, int sy, float2 e, float gx, float gy,
                                                uint32_t phx, uint32_t by, float lx0, float ly0,
                                                const TrialConst &tc) {
@@ -162,6 +166,22 @@ __device__ __forceinline__ float2 correct_ssb2(float2 g, int sy, float2 e, float
     __sincosf((float)(int32_t)ph * 1.4629180792671596e-09f, &sb, &cb);  // 2 pi ph / 2^32
     const float inv = rsqrtf(d2);
     return cmul(g, cmul(make_float2(dx * inv, -dy * inv), make_float2(cb, sb)));
+}
+
+// SSB1 correction of one G value, F = e^{iB} conj(E) where a(alpha_k - lambda Q') > 0 and 0
+// elsewhere (the caller handles DC and a_k = 0): chi(alpha_k) - chi(alpha_k - lambda Q') =
+// B - chi(lambda Q'), the same separable terms as correct_ssb2.
+__device__ __forceinline__ float2 correct_ssb1(float2 g, int sy, float2 e, float gx, float gy,
+                                               uint32_t phx, uint32_t by, float lx0, float ly0,
+                                               const TrialConst &tc) {
+    const float fsy = (float)sy;
+    const float lx = fmaf(tc.lxy, fsy, lx0), ly = fmaf(tc.lyy, fsy, ly0);
+    const float dmx = gx - lx, dmy = gy - ly;
+    if (!(aperture_r2(fmaf(dmx, dmx, dmy * dmy), tc) > 0.0f)) return make_float2(0.0f, 0.0f);
+    const uint32_t ph = phx + by * (uint32_t)sy;
+    float sb, cb;
+    __sincosf((float)(int32_t)ph * 1.4629180792671596e-09f, &sb, &cb);  // 2 pi ph / 2^32
+    return cmul(g, cmul(make_float2(cb, sb), cconj(e)));
 }
 
 // Phase atan2(y, x) in (-pi, pi]: octant reduction to a = min/max in [0, 1], an odd
@@ -184,42 +204,6 @@ __device__ __forceinline__ float fast_atan2(float y, float x) {
     if (ay > ax) r = 1.57079632679489662f - r;
     if (x < 0.0f) r = 3.14159265358979324f - r;
     return copysignf(r, y);
-}
-
-// Correction factor F_k(Q) such that C_k(Q) = G_k(Q) F_k(Q).
-//
-// With chi quadratic, chi(alpha_k -+ lambda Q') = chi(alpha_k) + chi(lambda Q') -+ B with
-// B = 2 pi alpha_k^T M Q' linear in Q (M the aberration matrix), so
-//   Gamma_k = a_k e^{-iB} [a_- e^{i chiQ} - a_+ e^{-i chiQ}] = a_k e^{-iB} D,
-//   D = (a_- - a_+) cos chiQ + i (a_- + a_+) sin chiQ,
-// and conj(Gamma)/|Gamma| = e^{iB} conj(D)/|D| (an exact rewriting).  chiQ comes from the
-// per-trial table E = e^{i chiQ}; B is carried exactly as a 32-bit fixed-point fraction of
-// a turn, b_x sx + b_y sy mod 2^32, so its range reduction is exact.
-// SSB1: F = e^{i(chi(alpha_k) - chi(alpha_k - lambda Q'))} = e^{iB} conj(E), masked by
-// a_k a_- > 0.  F(0) = 1 (the DC term is kept).  geo = (alpha_x, alpha_y, a_k, -).
-template <int N>
-__device__ __forceinline__ float2 correction_factor(int ny, int nx, float4 geo, uint2 bturn,
-                                                    float2 e, const TrialConst &tc) {
-    if ((nx | ny) == 0) return make_float2(1.0f, 0.0f);
-    if (!(geo.z > 0.0f)) return make_float2(0.0f, 0.0f);
-    const int sx = signed_bin<N>(nx), sy = signed_bin<N>(ny);
-    const float fx = (float)sx * tc.inv_nstep, fy = (float)sy * tc.inv_nstep;
-    const float lx = tc.lam * fmaf(tc.cr, fx, -tc.sr * fy);
-    const float ly = tc.lam * fmaf(tc.sr, fx, tc.cr * fy);
-    const float am = soft_aperture(geo.x - lx, geo.y - ly, tc.semi, tc.inv_dalpha);
-    const uint32_t ph = bturn.x * (uint32_t)sx + bturn.y * (uint32_t)sy;
-    float sb, cb;
-    sincospif((float)(int32_t)ph * 4.656612873077393e-10f, &sb, &cb);  // 2 pi ph / 2^32
-    if (tc.mode == 1) {
-        if (!(am > 0.0f)) return make_float2(0.0f, 0.0f);
-        return cmul(make_float2(cb, sb), cconj(e));
-    }
-    const float ap = soft_aperture(geo.x + lx, geo.y + ly, tc.semi, tc.inv_dalpha);
-    const float dx = (am - ap) * e.x, dy = (am + ap) * e.y;
-    const float d2 = fmaf(dx, dx, dy * dy);
-    if (!(d2 > 0.0f)) return make_float2(0.0f, 0.0f);
-    const float inv = rsqrtf(d2);
-    return cmul(make_float2(dx * inv, -dy * inv), make_float2(cb, sb));
 }
 
 }  // namespace ssb

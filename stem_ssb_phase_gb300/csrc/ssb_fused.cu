@@ -69,31 +69,37 @@ struct FusedParams {
     TrialConst tc;
 };
 
-template <int N>
+// Shapes of the fused kernel.  SSB2 (anti-Hermitian spectrum): the N/2 + 1 half-plane
+// columns, rows rebuilt by the C2R split into N/2-point transforms.  SSB1 (no symmetry):
+// all N columns and full N-point complex row transforms.
+template <int N, bool SSB1 = false>
 struct FusedShape {
-    static constexpr int T = N / kPts;              // threads per transform
+    static constexpr int T = N / kPts;              // threads per transform (rows and columns)
     static constexpr int GROUPS = kFusedThreads / T;  // transforms per block
-    static constexpr int H = N / 2 + 1;             // half-plane columns
-    static constexpr int M = N / 2;                 // row transforms: M-point complex IFFT
+    static constexpr int H = SSB1 ? N : N / 2 + 1;  // columns corrected and column-transformed
+    static constexpr int M = SSB1 ? N : N / 2;      // row transform length
+    static constexpr int RE = SSB1 ? kPts : 8;      // row transform points per thread (M / T)
     static constexpr int CW = GROUPS * kColsPerWarp;  // columns per column task
     static constexpr int RT = GROUPS < N ? GROUPS : N;  // rows per row task (multiple of 4)
     static constexpr int CT = (H + CW - 1) / CW;    // column tasks per plane
     static constexpr int NR = N / RT;               // row tasks per trial
     static constexpr int SMF = RegFFT<N, kPts>::SMEM;  // FFT scratch per group
-    static constexpr int LDZ = (H + 7) / 8 * 8;     // h row stride (64 B multiple)
+    static constexpr int LDZ = (N / 2 + 1 + 7) / 8 * 8;  // h row stride (64 B multiple)
     static constexpr int RC = RT / 2;               // 16-byte chunks per column segment
-    static constexpr int LDC = RT + 2;              // staged column-segment stride (16-B multiple)
+    // staged column-segment stride: SSB2 pads by one chunk; SSB1 (twice the columns) keeps
+    // segments dense and places chunk c of column nx at c xor (nx mod RC) instead
+    static constexpr int LDC = SSB1 ? RT : RT + 2;
     // dynamic shared memory layout, in float2 units.  A block runs one task at a time, so
     // the column task's FFT scratch and the row task's scratch + staged planes share OFF_U.
-    static constexpr int SMR = RegFFT<M, 8>::SMEM;                  // row FFT scratch per group
+    static constexpr int SMR = RegFFT<M, RE>::SMEM;                 // row FFT scratch per group
     static constexpr int OFF_TW = 0;                                // padded twiddles
-    static constexpr int OFF_TW2 = OFF_TW + (PadLen<N>::value + 1) / 2 * 2;  // M-point table
-    static constexpr int OFF_RED = OFF_TW2 + (PadLen<M>::value + 1) / 2 * 2;  // warp partials
+    static constexpr int OFF_TW2 = OFF_TW + (PadLen<N>::value + 1) / 2 * 2;  // N/2-point table
+    static constexpr int OFF_RED = OFF_TW2 + (PadLen<N / 2>::value + 1) / 2 * 2;  // partials
     static constexpr int OFF_U = OFF_RED + 16;
     static constexpr int OFF_FFT = OFF_U;                           // column task: [GROUPS][SMF]
     static constexpr int OFF_RFFT = OFF_U;                          // row task: [GROUPS][SMR]
     static constexpr int OFF_TILE = OFF_RFFT + (GROUPS * SMR + 1) / 2 * 2;  // [2][TILEBUF]
-    static constexpr int TILEBUF = H * LDC + LDZ + M;               // segments, h, Rp
+    static constexpr int TILEBUF = SSB1 ? H * LDC : H * LDC + LDZ + M;  // segments (, h, Rp)
     static constexpr int U_COL = GROUPS * SMF;
     static constexpr int U_ROW = OFF_TILE - OFF_U + 2 * TILEBUF;
     static constexpr int TOTAL = OFF_U + (U_COL > U_ROW ? U_COL : U_ROW);
@@ -185,10 +191,13 @@ __device__ void nyquist_transform(const FusedParams &p, float2 *fsm, const float
 // once all of them have.  Each warp reads the count when the task starts and checks it
 // before its first ring write, so the load's latency hides behind the column work.
 // Returns, uniform over the warp, whether the warp could write the slot.
-template <int N>
+// SSB1 covers all N columns; column nx > N/2 reads the cache's column N - nx at the
+// mirrored rows, conjugated (G(-Q) = conj G(Q)).
+template <int N, bool SSB1>
 __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
                            const unsigned *free_word, unsigned *err) {
-    using S = FusedShape<N>;
+    using S = FusedShape<N, SSB1>;
+    constexpr int HG = N / 2 + 1;  // columns of the half-plane G cache
     const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T, lane = tid & 31;
     const int kk = idx / S::CT, ct = idx - kk * S::CT;
     const int k = b * p.Bk + kk;
@@ -203,23 +212,30 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
         const int nx = ct * S::CW + c * S::GROUPS + grp;
         const bool valid = nx < S::H;
         const int sx = nx < N / 2 ? nx : nx - N;
-        // Columns with exactly zero transfer (both shifted apertures miss the whole column;
-        // every column but DC for an inactive BF pixel) skip the loads, the correction and
-        // the transform and store zeros.  The decision is uniform over the warp.
-        const bool zero = nx > 0 && (!(geo.z > 0.0f) || column_zero(sx, geo.x, geo.y, p.tc));
+        // Columns with exactly zero transfer (SSB2: both shifted apertures miss the whole
+        // column; SSB1: the aperture at alpha_k - lambda Q' does; every column but DC for an
+        // inactive BF pixel) skip the loads, the correction and the transform and store
+        // zeros.  The decision is uniform over the warp.
+        const bool zero = nx > 0 && (!(geo.z > 0.0f) || (SSB1 ? column_zero1(sx, geo.x, geo.y, p.tc)
+                                                               : column_zero(sx, geo.x, geo.y, p.tc)));
         const bool skip = __all_sync(0xffffffffu, zero || !valid);
         float2 v[kPts];
         float2 hval = make_float2(0.f, 0.f);
-        bool hstore = skip && j == 0 && nx >= 1 && nx < N / 2;  // h = 0 there
+        bool hstore = !SSB1 && skip && j == 0 && nx >= 1 && nx < N / 2;  // h = 0 there
         if (valid && !skip) {
-            const float2 *g = p.G + ((size_t)k * S::H + nx) * N + j;
             const float2 *e = p.Et + (size_t)nx * N + j;
             float2 ev[kPts];
+            if (!SSB1 || nx <= N / 2) {
+                const float2 *g = p.G + ((size_t)k * HG + nx) * N + j;
 #pragma unroll
-            for (int r = 0; r < kPts; ++r) {
-                v[r] = __ldcs(g + S::T * r);
-                ev[r] = __ldg(e + S::T * r);
+                for (int r = 0; r < kPts; ++r) v[r] = __ldcs(g + S::T * r);
+            } else {  // G(ny, nx) = conj G(N - ny, N - nx), row indices mod N
+                const float2 *g = p.G + ((size_t)k * HG + (N - nx)) * N;
+#pragma unroll
+                for (int r = 0; r < kPts; ++r) v[r] = cconj(__ldcs(g + ((N - j - S::T * r) & (N - 1))));
             }
+#pragma unroll
+            for (int r = 0; r < kPts; ++r) ev[r] = __ldg(e + S::T * r);
             const float lx0 = p.tc.lxs * (float)sx, ly0 = p.tc.lys * (float)sx;
             const uint32_t phx = bt.x * (uint32_t)sx;
             const bool active = geo.z > 0.0f;  // a(alpha_k) = 0: only the DC term survives
@@ -228,10 +244,12 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
                 const int ny = j + S::T * r;
                 const int sy = ny < N / 2 ? ny : ny - N;
                 const float2 gv = v[r];
-                float2 cv = active ? correct_ssb2(gv, sy, ev[r], geo.x, geo.y, phx, bt.y, lx0, ly0, p.tc)
-                                   : make_float2(0.f, 0.f);
+                float2 cv = make_float2(0.f, 0.f);
+                if (active)
+                    cv = SSB1 ? correct_ssb1(gv, sy, ev[r], geo.x, geo.y, phx, bt.y, lx0, ly0, p.tc)
+                              : correct_ssb2(gv, sy, ev[r], geo.x, geo.y, phx, bt.y, lx0, ly0, p.tc);
                 if ((nx | ny) == 0) cv = gv;  // C(0) = G(0)
-                if (r == kPts / 2 && j == 0 && nx >= 1 && nx < N / 2) {
+                if (!SSB1 && r == kPts / 2 && j == 0 && nx >= 1 && nx < N / 2) {
                     // Nyquist row (ny = N/2): the mirror bin N - nx has no partner and
                     // carries its own correction, at signed bins (-nx, -N/2)
                     const float2 em = __ldg(p.Et + (size_t)(N - nx) * N + N / 2);
@@ -267,17 +285,23 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
 
 // ---------------------------------------------------------------- row task
 
-// Start the asynchronous copy of one plane's RT-row segment of every half-plane column
-// (RT consecutive values, contiguous in the column-major ring), of its Nyquist terms h
-// and of its Nyquist-row transform Rp.
-template <int N>
+// Start the asynchronous copy of one plane's RT-row segment of every transformed column
+// (RT consecutive values, contiguous in the column-major ring) and, for SSB2, of its
+// Nyquist terms h and of its Nyquist-row transform Rp.  SSB1 places 16-byte chunk c of
+// column nx at chunk c xor (nx mod RC) of the column's dense segment.
+template <int N, bool SSB1>
 __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk, int ry0,
                                           float2 *buf) {
-    using S = FusedShape<N>;
+    using S = FusedShape<N, SSB1>;
     const float2 *zsrc = p.Z + ((size_t)slot * p.Bk + kk) * S::H * N + ry0;
     for (int e = threadIdx.x; e < S::H * S::RC; e += kFusedThreads) {
         const int nx = e / S::RC, c = e - nx * S::RC;
-        cp_async16(buf + nx * S::LDC + 2 * c, zsrc + (size_t)nx * N + 2 * c);
+        const int cd = SSB1 ? (c ^ (nx & (S::RC - 1))) : c;
+        cp_async16(buf + nx * S::LDC + 2 * cd, zsrc + (size_t)nx * N + 2 * c);
+    }
+    if (SSB1) {
+        cp_async_commit();
+        return;
     }
     const float2 *hsrc = p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ;
     for (int e = threadIdx.x; e < S::LDZ / 2; e += kFusedThreads)
@@ -294,10 +318,11 @@ __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk
 //          V(m) = Y(m) + conj Y(N/2-m) + i (Y(m) - conj Y(N/2-m)) e^{2 pi i m/N},
 //          whose output holds Im c at pixels 2j (real part) and 2j+1 (imaginary part);
 //   Re c = Re Z(0) + (-1)^rx Re Z(N/2) + s Rp(rx),   s = (-1)^ry.
-template <int N, bool OBJ>
+// SSB1 row ry: one N-point complex IFFT of the staged row, c at pixels j + T r.
+template <int N, bool OBJ, bool SSB1>
 __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int planes,
-                             unsigned *plane_free, unsigned *chain, unsigned *err, int *s_ok) {
-    using S = FusedShape<N>;
+                         unsigned *plane_free, unsigned *chain, unsigned *err, int *s_ok) {
+    using S = FusedShape<N, SSB1>;
     const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
     const int slot = b % p.D;
     const int ry0 = rt * S::RT;
@@ -315,12 +340,12 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         acc1[r] = 0.f;
         acco[r] = make_float2(0.f, 0.f);
     }
-    row_issue<N>(p, slot, 0, ry0, tiles);
+    row_issue<N, SSB1>(p, slot, 0, ry0, tiles);
     for (int kk = 0; kk < planes; ++kk) {
         float2 *cur = tiles + (kk & 1) * S::TILEBUF;
         __syncthreads();  // everyone is done with the other buffer (plane kk - 1)
         if (kk + 1 < planes) {
-            row_issue<N>(p, slot, kk + 1, ry0, tiles + ((kk + 1) & 1) * S::TILEBUF);
+            row_issue<N, SSB1>(p, slot, kk + 1, ry0, tiles + ((kk + 1) & 1) * S::TILEBUF);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
@@ -332,42 +357,60 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             // completed (their data is in shared memory), so no fence is needed here.
             red_relaxed_add(plane_free + (size_t)b * p.Bk + kk, 1u);
         }
-        const float2 *seg = cur + lr;               // element (nx, lr) at seg[nx * LDC]
-        const float2 *hs = cur + S::H * S::LDC;
-        const float2 *rp = hs + S::LDZ;
-        const float2 z0 = seg[0], zm = seg[S::M * S::LDC];
-        float2 v[8];
+        if constexpr (SSB1) {
+            float2 v[kPts];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int m = j + S::T * r, mc = S::M - m;
-            float2 ym, yc;
-            if (m == 0) {
-                ym = make_float2(z0.y, 0.f);
-                yc = make_float2(zm.y, 0.f);
-            } else {
-                const float2 za = seg[m * S::LDC], ha = hs[m];
-                const float2 zb = seg[mc * S::LDC], hb = hs[mc];
-                ym = make_float2(fmaf(-sg, ha.y, za.y), fmaf(sg, ha.x, -za.x));
-                yc = make_float2(fmaf(-sg, hb.y, zb.y), fmaf(sg, hb.x, -zb.x));
+            for (int r = 0; r < kPts; ++r) {
+                const int nx = j + S::T * r;  // element (nx, lr): chunk lr / 2 of column nx, swizzled
+                v[r] = active ? cur[nx * S::LDC + 2 * ((lr >> 1) ^ (nx & (S::RC - 1))) + (lr & 1)]
+                              : make_float2(0.f, 0.f);
             }
-            const float2 a = make_float2(ym.x + yc.x, ym.y - yc.y);
-            const float2 bb = cmul(make_float2(ym.x - yc.x, ym.y + yc.y), twid<+1>(twN, lay(m)));
-            v[r] = active ? make_float2(a.x - bb.y, a.y + bb.x) : make_float2(0.f, 0.f);
-        }
-        reg_fft<S::M, 8, +1>(v, smem + S::OFF_RFFT + grp * S::SMR, smem + S::OFF_TW2, j, warp_bar);
-        const float re_even = z0.x + zm.x, re_odd = z0.x - zm.x;
+            reg_fft<N, kPts, +1>(v, smem + S::OFF_RFFT + grp * S::SMR, twN, j, warp_bar);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const float2 rpv = rp[j + S::T * r];
-            const float re0 = fmaf(sg, rpv.x, re_even), re1 = fmaf(sg, rpv.y, re_odd);
-            const float p0 = fast_atan2(v[r].x, re0), p1 = fast_atan2(v[r].y, re1);
-            acc1[2 * r] += p0;
-            acc1[2 * r + 1] += p1;
-            acc2 = fmaf(p0, p0, acc2);
-            acc2 = fmaf(p1, p1, acc2);
-            if (OBJ) {
-                acco[2 * r] = cadd(acco[2 * r], make_float2(re0, v[r].x));
-                acco[2 * r + 1] = cadd(acco[2 * r + 1], make_float2(re1, v[r].y));
+            for (int r = 0; r < kPts; ++r) {
+                const float ph = fast_atan2(v[r].y, v[r].x);
+                acc1[r] += ph;
+                acc2 = fmaf(ph, ph, acc2);
+                if (OBJ) acco[r] = cadd(acco[r], v[r]);
+            }
+        } else {
+            const float2 *seg = cur + lr;               // element (nx, lr) at seg[nx * LDC]
+            const float2 *hs = cur + S::H * S::LDC;
+            const float2 *rp = hs + S::LDZ;
+            const float2 z0 = seg[0], zm = seg[S::M * S::LDC];
+            float2 v[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int m = j + S::T * r, mc = S::M - m;
+                float2 ym, yc;
+                if (m == 0) {
+                    ym = make_float2(z0.y, 0.f);
+                    yc = make_float2(zm.y, 0.f);
+                } else {
+                    const float2 za = seg[m * S::LDC], ha = hs[m];
+                    const float2 zb = seg[mc * S::LDC], hb = hs[mc];
+                    ym = make_float2(fmaf(-sg, ha.y, za.y), fmaf(sg, ha.x, -za.x));
+                    yc = make_float2(fmaf(-sg, hb.y, zb.y), fmaf(sg, hb.x, -zb.x));
+                }
+                const float2 a = make_float2(ym.x + yc.x, ym.y - yc.y);
+                const float2 bb = cmul(make_float2(ym.x - yc.x, ym.y + yc.y), twid<+1>(twN, lay(m)));
+                v[r] = active ? make_float2(a.x - bb.y, a.y + bb.x) : make_float2(0.f, 0.f);
+            }
+            reg_fft<S::M, 8, +1>(v, smem + S::OFF_RFFT + grp * S::SMR, smem + S::OFF_TW2, j, warp_bar);
+            const float re_even = z0.x + zm.x, re_odd = z0.x - zm.x;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float2 rpv = rp[j + S::T * r];
+                const float re0 = fmaf(sg, rpv.x, re_even), re1 = fmaf(sg, rpv.y, re_odd);
+                const float p0 = fast_atan2(v[r].x, re0), p1 = fast_atan2(v[r].y, re1);
+                acc1[2 * r] += p0;
+                acc1[2 * r + 1] += p1;
+                acc2 = fmaf(p0, p0, acc2);
+                acc2 = fmaf(p1, p1, acc2);
+                if (OBJ) {
+                    acco[2 * r] = cadd(acco[2 * r], make_float2(re0, v[r].x));
+                    acco[2 * r + 1] = cadd(acco[2 * r + 1], make_float2(re1, v[r].y));
+                }
             }
         }
     }
@@ -376,7 +419,33 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
     // which keeps the per-pixel summation order fixed while the tasks themselves overlap.
     if (tid == 0) *s_ok = wait_at_least(chain + rt, (unsigned)b, err);
     __syncthreads();
-    if (active && *s_ok) {
+    if (SSB1 && active && *s_ok) {
+        // pixel j + T r of row ry holds acc1[r]; loads are issued in groups ahead of their
+        // stores (a store through the same pointer would hold back each following load)
+        constexpr int GS = OBJ ? 4 : 16;
+        double *s1 = p.S1 + (size_t)ry * N + j;
+#pragma unroll
+        for (int g0 = 0; g0 < 16; g0 += GS) {
+            double old[GS];
+#pragma unroll
+            for (int r = 0; r < GS; ++r) old[r] = __ldcg(s1 + S::T * (g0 + r));
+#pragma unroll
+            for (int r = 0; r < GS; ++r) s1[S::T * (g0 + r)] = old[r] + (double)acc1[g0 + r];
+        }
+        if (OBJ) {
+            double2 *os = p.Osum + (size_t)ry * N + j;
+#pragma unroll
+            for (int g0 = 0; g0 < 16; g0 += 4) {
+                double2 o[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) o[r] = __ldcg(os + S::T * (g0 + r));
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    os[S::T * (g0 + r)] = make_double2(o[r].x + acco[g0 + r].x, o[r].y + acco[g0 + r].y);
+            }
+        }
+    }
+    if (!SSB1 && active && *s_ok) {
         // Loads are issued in groups ahead of their stores: a store through the same
         // pointer would otherwise hold back each following load for a full round trip.
         // A thread owns pixel pairs (2 (j + T r), 2 (j + T r) + 1).  With the object sums
@@ -432,9 +501,9 @@ __device__ __forceinline__ int planes_in(const FusedParams &p, int b) {
 
 // Ticket t -> task.  Phase 0 = columns of batch 0; phase q (1 <= q < nbatch) = columns
 // of batch q then rows of batch q-1; phase nbatch = rows of the last batch.
-template <int N>
+template <int N, bool SSB1>
 __device__ Task decode_ticket(const FusedParams &p, unsigned t) {
-    using S = FusedShape<N>;
+    using S = FusedShape<N, SSB1>;
     const unsigned nc_full = (unsigned)p.Bk * S::CT;
     const unsigned nc_last = (unsigned)planes_in(p, p.nbatch - 1) * S::CT;
     const unsigned nr = S::NR;
@@ -459,9 +528,9 @@ __device__ Task decode_ticket(const FusedParams &p, unsigned t) {
     return Task{2, 0, 0};
 }
 
-template <int N, bool OBJ>
+template <int N, bool OBJ, bool SSB1>
 __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(FusedParams p) {
-    using S = FusedShape<N>;
+    using S = FusedShape<N, SSB1>;
     extern __shared__ __align__(16) float2 smem[];
     __shared__ unsigned s_ticket;
     __shared__ int s_ok;
@@ -481,28 +550,33 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(Fuse
     if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
     while (true) {
         __syncthreads();
-        const Task task = decode_ticket<N>(p, s_ticket);
+        const Task task = decode_ticket<N, SSB1>(p, s_ticket);
         if (task.kind == 2) break;
         if (task.kind == 0) {
             const int kk = task.idx / S::CT;
             // this plane of the ring slot was last read by the row tasks of batch b - D
             const unsigned *free_word =
                 task.b >= p.D ? plane_free + (size_t)(task.b - p.D) * p.Bk + kk : nullptr;
-            const int ok = column_task<N>(p, smem, task.b, task.idx, free_word, err);
+            const int ok = column_task<N, SSB1>(p, smem, task.b, task.idx, free_word, err);
             __syncthreads();
             if (tid == 0) {
                 // the next ticket's round trip overlaps the fence
                 const unsigned next = atomicAdd(ticket, 1u);
                 fence_acq_rel();  // publishes the task's ring columns and Nyquist terms
-                // The task that completes the plane's column pass also transforms the
+                // SSB2: the task that completes the plane's column pass also transforms the
                 // plane's Nyquist terms (it acquires the others' h with the count).
-                const unsigned done = atom_add_acq_rel(h_cnt + (size_t)task.b * p.Bk + kk, 1u) + 1u;
-                s_nyq = done == (unsigned)S::CT;
+                if (SSB1) {
+                    s_nyq = 0;
+                } else {
+                    const unsigned done =
+                        atom_add_acq_rel(h_cnt + (size_t)task.b * p.Bk + kk, 1u) + 1u;
+                    s_nyq = done == (unsigned)S::CT;
+                }
                 if (!s_nyq) red_relaxed_add(col_done + task.b, 1u);
                 s_ticket = next;
             }
             __syncthreads();
-            if (s_nyq) {
+            if (!SSB1 && s_nyq) {
                 if (tid < 32 && ok)  // whole warp: the transform synchronises the warp
                     nyquist_transform<N>(p, smem + S::OFF_FFT + (tid / S::T) * S::SMF,
                                          smem + S::OFF_TW, smem + S::OFF_TW2, task.b % p.D, kk,
@@ -518,8 +592,8 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(Fuse
                 s_ok = wait_at_least(col_done + task.b, (unsigned)(planes_in(p, task.b) * S::CT), err);
             __syncthreads();
             if (s_ok) {
-                row_task<N, OBJ>(p, smem, task.b, task.idx, planes_in(p, task.b), plane_free,
-                                 chain, err, &s_ok);
+                row_task<N, OBJ, SSB1>(p, smem, task.b, task.idx, planes_in(p, task.b), plane_free,
+                                       chain, err, &s_ok);
             } else if (tid == 0) {  // release the planes anyway so that no wait is left behind
                 for (int kk = 0; kk < planes_in(p, task.b); ++kk)
                     atomicAdd(plane_free + (size_t)task.b * p.Bk + kk, 1u);
@@ -569,38 +643,40 @@ size_t fused_sync_words(int N, int n_bf, int Bk) {
 }
 
 static size_t ldz_for(int N) { return (size_t)((N / 2 + 1 + 7) / 8 * 8); }
-size_t fused_ring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)N * (N / 2 + 1); }
+size_t fused_ring_elems(int N, int Bk, int D, bool ssb1) {
+    return (size_t)D * Bk * (size_t)N * (ssb1 ? N : N / 2 + 1);
+}
 size_t fused_hring_elems(int N, int Bk, int D) { return (size_t)D * Bk * ldz_for(N); }
 size_t fused_rring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)(N / 2); }
 int fused_row_tasks(int N) { return row_tasks_for(N); }
 
-template <int N, bool OBJ>
+template <int N, bool OBJ, bool SSB1>
 static cudaError_t fused_launch(const FusedParams &fp, cudaStream_t s) {
-    using S = FusedShape<N>;
+    using S = FusedShape<N, SSB1>;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(k_fused<N, OBJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(k_fused<N, OBJ, SSB1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)S::BYTES)) != cudaSuccess)
         return e;
     int dev = 0, sms = 0, per_sm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fused<N, OBJ>, kFusedThreads,
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fused<N, OBJ, SSB1>, kFusedThreads,
                                                            S::BYTES)) != cudaSuccess)
         return e;
     const long tickets = (long)fp.nbatch * (fp.Bk * S::CT + S::NR);
     const int grid = (int)std::max(1L, std::min((long)sms * std::max(per_sm, 1), tickets));
     prof_begin("k_fused", s);
-    k_fused<N, OBJ><<<grid, kFusedThreads, S::BYTES, s>>>(fp);
+    k_fused<N, OBJ, SSB1><<<grid, kFusedThreads, S::BYTES, s>>>(fp);
     prof_end(s);
     count_launch();
     return cudaGetLastError();
 }
 
-template <int N>
+template <int N, bool SSB1>
 static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th, double *loss_slot,
                                      bool want_object, cudaStream_t s) {
-    using S = FusedShape<N>;
+    using S = FusedShape<N, SSB1>;
     cudaError_t e;
     if ((e = launch_theta_tables(a, th, s)) != cudaSuccess) return e;
     const size_t P = (size_t)N * N;
@@ -630,7 +706,7 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     fp.nbatch = nbatch;
     fp.D = a.D;
     fp.tc = make_trial_const(a, th, N);
-    e = want_object ? fused_launch<N, true>(fp, s) : fused_launch<N, false>(fp, s);
+    e = want_object ? fused_launch<N, true, SSB1>(fp, s) : fused_launch<N, false, SSB1>(fp, s);
     if (e != cudaSuccess) return e;
     prof_begin("k_loss", s);
     k_loss_fused<<<1, 1024, 0, s>>>(a.S1, a.S2g, S::NR, (int)P, 1.0 / a.n_bf, loss_slot);
@@ -642,12 +718,18 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
 cudaError_t run_objective_fused(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,
                                 bool want_object, cudaStream_t s) {
     const TrialHost th = trial_host(theta);
+    const bool s1 = a.mode == 1;
     switch (a.N) {
-        case 32: return fused_objective_n<32>(a, th, loss_slot, want_object, s);
-        case 64: return fused_objective_n<64>(a, th, loss_slot, want_object, s);
-        case 128: return fused_objective_n<128>(a, th, loss_slot, want_object, s);
-        case 256: return fused_objective_n<256>(a, th, loss_slot, want_object, s);
-        case 512: return fused_objective_n<512>(a, th, loss_slot, want_object, s);
+        case 32: return s1 ? fused_objective_n<32, true>(a, th, loss_slot, want_object, s)
+                           : fused_objective_n<32, false>(a, th, loss_slot, want_object, s);
+        case 64: return s1 ? fused_objective_n<64, true>(a, th, loss_slot, want_object, s)
+                           : fused_objective_n<64, false>(a, th, loss_slot, want_object, s);
+        case 128: return s1 ? fused_objective_n<128, true>(a, th, loss_slot, want_object, s)
+                            : fused_objective_n<128, false>(a, th, loss_slot, want_object, s);
+        case 256: return s1 ? fused_objective_n<256, true>(a, th, loss_slot, want_object, s)
+                            : fused_objective_n<256, false>(a, th, loss_slot, want_object, s);
+        case 512: return s1 ? fused_objective_n<512, true>(a, th, loss_slot, want_object, s)
+                            : fused_objective_n<512, false>(a, th, loss_slot, want_object, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -45,9 +45,7 @@ struct ObjectiveArgs {
     uint2 *kturn;           // [n_bf] per-trial B slopes (32-bit turn fractions)
     float2 *E;              // [N][N] per-trial e^{i chi(lambda Q')}
     const float2 *tw;       // [N] twiddles exp(+2 pi i m/N)
-    float2 *X;              // [B][N][N] column-pass intermediate
-    int B;                  // BF batch
-    double *S1, *S2;        // [N][N] float64 accumulators
+    double *S1;             // [N][N] float64 sum of phases
     double2 *Osum;          // [N][N] float64 object accumulator (nullable)
     double *loss;           // device float64, one per trial slot
     // fused (persistent) path
@@ -70,16 +68,15 @@ cudaError_t launch_theta_tables(const ObjectiveArgs &a, const TrialHost &th, cud
 
 // persistent fused path (SSB2): sizes of its buffers and the evaluation itself
 size_t fused_sync_words(int N, int n_bf, int Bk);
-size_t fused_ring_elems(int N, int Bk, int D);
+size_t fused_ring_elems(int N, int Bk, int D, bool ssb1 = false);  // ssb1: all N columns
 size_t fused_hring_elems(int N, int Bk, int D);
 size_t fused_rring_elems(int N, int Bk, int D);
 int fused_row_tasks(int N);
+// One full objective evaluation on the persistent fused kernel (accumulators and
+// scheduler words cleared first), loss written to *loss_slot.
 cudaError_t run_objective_fused(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,
                                 bool want_object, cudaStream_t s);
 
-// Run one full objective evaluation (S1/S2 zeroed first), loss written to *loss_slot.
-cudaError_t run_objective(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,
-                          bool want_object, cudaStream_t s);
 // mean phase = S1/n_bf (float32), object = Osum * scale (complex64) if out_obj != nullptr
 cudaError_t launch_finalize(const ObjectiveArgs &a, float *mean_phase, float *out_obj,
                             cudaStream_t s);

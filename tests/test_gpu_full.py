@@ -1,4 +1,4 @@
-"""Parity at the full size the benchmark times: 512 x 512 scan, 192 x 192 detector, all
+"""Parity at the full size the benchmark times (and the SSB1 transfer at the same size): 512 x 512 scan, 192 x 192 detector, all
 8,937 BF pixels, uint32 counts (mean 1,000), generated on the GPU exactly as bench.py
 does, evaluated through the C ABI in the benchmark's launch configuration, and compared
 with the float64 oracle run over every BF pixel in spawned processes on the host cores.
@@ -53,3 +53,24 @@ def test_full_size_batch_equals_scalar_calls(full_case):
     assert np.array_equal(ctx.loss_batch(thetas), batch)  # run to run
     # the generating aberrations give the smallest loss of the three
     assert int(np.argmin(batch)) == 0
+
+
+def test_full_size_ssb1_matches_the_oracle(full_case):
+    """The SSB1 transfer at full size: all 512 columns and full complex row transforms."""
+    w, geom, host, _ = full_case
+    import stem_ssb_phase_gb300 as m
+    theta = ssb_synth.draw_trials(w, 1)[0]
+    ctx = m.SSB(geom, host, transfer="ssb1")
+    try:
+        mp, _, loss = ctx.reconstruct(theta, want_object=False)
+        batch = ctx.loss_batch(np.array(theta)[None])
+    finally:
+        ctx.close()
+    assert batch[0] == loss
+    ref = oracle.objective(geom, theta, counts=host, mode="ssb1",
+                           workers=min(32, oracle.default_workers()))
+    assert abs(loss - ref["loss"]) <= 1e-5 * ref["loss"], (loss, ref["loss"])
+    mask = ~ref["branch_cut"]
+    err = np.abs(mp.cpu().numpy().astype(np.float64) - ref["mean_phase"])[mask]
+    assert mask.mean() > 0.9
+    assert err.max() <= 1e-4, (err.max(), int((err > 1e-4).sum()))

@@ -111,13 +111,14 @@ def test_tiny_objective(ssbgpu, tiny_data, transfer):
     assert abs(loss - ref["loss"]) <= LOSS_RTOL * ref["loss"]
 
 
-def test_small_batch_of_trials(ssbgpu, small_data):
+@pytest.mark.parametrize("transfer", ["ssb2", "ssb1"])
+def test_small_batch_of_trials(ssbgpu, small_data, transfer):
     w, geom, counts, _ = small_data
-    ctx = ssbgpu.SSB(geom, counts)
+    ctx = ssbgpu.SSB(geom, counts, transfer=transfer)
     thetas = ssb_synth.draw_trials(w, w.n_trials)
     gpu = ctx.loss_batch(thetas)
     for th, lg in zip(thetas[:4], gpu[:4]):
-        ref = oracle.objective(geom, th, counts=counts, workers=_workers())
+        ref = oracle.objective(geom, th, counts=counts, mode=transfer, workers=_workers())
         assert abs(lg - ref["loss"]) <= LOSS_RTOL * ref["loss"], (th, lg, ref["loss"])
     # batch entries equal single-trial calls bit for bit
     singles = np.array([ctx.loss(th) for th in thetas])
@@ -126,33 +127,43 @@ def test_small_batch_of_trials(ssbgpu, small_data):
     assert np.array_equal(ctx.loss_batch(thetas), gpu)
 
 
-def test_small_truth_phase_and_object(ssbgpu, small_data):
+@pytest.mark.parametrize("transfer", ["ssb2", "ssb1"])
+def test_small_truth_phase_and_object(ssbgpu, small_data, transfer):
     w, geom, counts, _ = small_data
-    ctx = ssbgpu.SSB(geom, counts)
+    ctx = ssbgpu.SSB(geom, counts, transfer=transfer)
     mp, obj, loss = ctx.reconstruct(w.truth)
-    ref = oracle.objective(geom, w.truth, counts=counts, want_object=True, workers=_workers())
+    ref = oracle.objective(geom, w.truth, counts=counts, mode=transfer, want_object=True,
+                           workers=_workers())
     assert abs(loss - ref["loss"]) <= LOSS_RTOL * ref["loss"]
     _check_phase(mp.cpu().numpy(), ref)
     o = obj.cpu().numpy().astype(np.complex128)
     assert np.linalg.norm(o - ref["object"]) <= 1e-5 * np.linalg.norm(ref["object"])
 
 
-@pytest.mark.slow
-def test_medium_objective(ssbgpu):
+@pytest.fixture(scope="module")
+def medium_data():
     w = ssb_synth.WORKLOADS["medium"]
     geom, counts, _ = ssb_synth.simulate_counts_numpy(w)
-    ctx = ssbgpu.SSB(geom, counts)
+    return w, geom, counts
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("transfer", ["ssb2", "ssb1"])
+def test_medium_objective(ssbgpu, medium_data, transfer):
+    w, geom, counts = medium_data
+    ctx = ssbgpu.SSB(geom, counts, transfer=transfer)
     thetas = np.vstack([np.array(w.truth)[None], ssb_synth.draw_trials(w, w.n_trials)])
     gpu = ctx.loss_batch(thetas)
     assert np.all(np.isfinite(gpu))
     for j in (0, 1, 2):
-        ref = oracle.objective(geom, thetas[j], counts=counts, workers=_workers())
+        ref = oracle.objective(geom, thetas[j], counts=counts, mode=transfer, workers=_workers())
         assert abs(gpu[j] - ref["loss"]) <= LOSS_RTOL * ref["loss"]
     # object redraw at the best trial
     best = thetas[int(np.argmin(gpu))]
     mp, obj, loss = ctx.reconstruct(best)
     assert loss == gpu[int(np.argmin(gpu))]
-    ref = oracle.objective(geom, best, counts=counts, want_object=True, workers=_workers())
+    ref = oracle.objective(geom, best, counts=counts, mode=transfer, want_object=True,
+                           workers=_workers())
     _check_phase(mp.cpu().numpy(), ref)
 
 
@@ -173,30 +184,32 @@ def test_single_bf_pixel(ssbgpu, tiny_data):
     _check_phase(mp.cpu().numpy(), refp)
 
 
-def test_inactive_bf_pixels_give_zero_phase(ssbgpu, tiny_data):
+@pytest.mark.parametrize("transfer", ["ssb2", "ssb1"])
+def test_inactive_bf_pixels_give_zero_phase(ssbgpu, tiny_data, transfer):
     w, geom, counts, _ = tiny_data
     # BF pixels at least 2 px off axis with a 1 mrad probe aperture: a(alpha_k) = 0
     r = np.hypot(geom.bf_det_yx[:, 0], geom.bf_det_yx[:, 1])
     sub = np.nonzero(r >= 2.0)[0]
     g2 = ssb_synth.make_geometry(w, bf_subset=sub)
     g2.semiangle_mrad = 1.0
-    ctx = ssbgpu.SSB(g2, counts[sub])
+    ctx = ssbgpu.SSB(g2, counts[sub], transfer=transfer)
     th = (50.0, 3.0, 0.2, 0.1)
-    assert oracle.objective(g2, th, counts=counts[sub])["loss"] == 0.0
+    assert oracle.objective(g2, th, counts=counts[sub], mode=transfer)["loss"] == 0.0
     assert ctx.loss(th) == 0.0
     mp, _, _ = ctx.reconstruct(th, want_object=False)
     assert float(mp.abs().max()) == 0.0
     # mixed: the inactive pixels stay in the normalisation
     g3 = ssb_synth.make_geometry(w)
     g3.semiangle_mrad = 4.0
-    ctx3 = ssbgpu.SSB(g3, counts)
-    ref = oracle.objective(g3, th, counts=counts)
+    ctx3 = ssbgpu.SSB(g3, counts, transfer=transfer)
+    ref = oracle.objective(g3, th, counts=counts, mode=transfer)
     assert abs(ctx3.loss(th) - ref["loss"]) <= LOSS_RTOL * ref["loss"]
 
 
+@pytest.mark.parametrize("transfer", ["ssb2", "ssb1"])
 @pytest.mark.parametrize("scan_n,det_n,radius,n_sub", [(64, 32, 8.0, None), (512, 192, 53.3, 24),
                                                       (256, 96, 27.0, 40)])
-def test_other_scan_sizes(ssbgpu, scan_n, det_n, radius, n_sub):
+def test_other_scan_sizes(ssbgpu, scan_n, det_n, radius, n_sub, transfer):
     w = ssb_synth.Workload("edge", scan_n, det_n, radius, "u32", 300.0, 0.2,
                            (-40.0, 12.0, 0.6, 0.2), seed=21, trial_seed=22, n_trials=1)
     sub = None
@@ -205,9 +218,9 @@ def test_other_scan_sizes(ssbgpu, scan_n, det_n, radius, n_sub):
         sub = np.linspace(0, n_all - 1, n_sub).astype(int)
     geom = ssb_synth.make_geometry(w, bf_subset=sub)
     _, counts, _ = ssb_synth.simulate_counts_numpy(w, geom=geom)
-    ctx = ssbgpu.SSB(geom, counts)
+    ctx = ssbgpu.SSB(geom, counts, transfer=transfer)
     th = (-30.0, 10.0, 0.5, 0.2)
-    ref = oracle.objective(geom, th, counts=counts, workers=_workers())
+    ref = oracle.objective(geom, th, counts=counts, mode=transfer, workers=_workers())
     assert abs(ctx.loss(th) - ref["loss"]) <= LOSS_RTOL * ref["loss"]
     mp, _, _ = ctx.reconstruct(th, want_object=False)
     _check_phase(mp.cpu().numpy(), ref)
