@@ -87,8 +87,12 @@ struct FusedShape {
     static constexpr int LDZ = (N / 2 + 1 + 7) / 8 * 8;  // h row stride (64 B multiple)
     static constexpr int RC = RT / 2;               // 16-byte chunks per column segment
     // staged column-segment stride: SSB2 pads by one chunk; SSB1 (twice the columns) keeps
-    // segments dense and places chunk c of column nx at c xor (nx mod RC) instead
+    // segments dense and places chunk c of column nx at c xor ((nx >> SWS) mod RC) instead.
+    // With 8-row segments two columns share a 128-byte bank row, so the xor follows nx / 2:
+    // 16 consecutive columns then cover 8 bank pairs (two-way conflicts, the least 16-byte
+    // chunks allow).
     static constexpr int LDC = SSB1 ? RT : RT + 2;
+    static constexpr int SWS = RT == 8 ? 1 : 0;
     // dynamic shared memory layout, in float2 units.  A block runs one task at a time, so
     // the column task's FFT scratch and the row task's scratch + staged planes share OFF_U.
     static constexpr int SMR = RegFFT<M, RE>::SMEM;                 // row FFT scratch per group
@@ -288,7 +292,7 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
 // Start the asynchronous copy of one plane's RT-row segment of every transformed column
 // (RT consecutive values, contiguous in the column-major ring) and, for SSB2, of its
 // Nyquist terms h and of its Nyquist-row transform Rp.  SSB1 places 16-byte chunk c of
-// column nx at chunk c xor (nx mod RC) of the column's dense segment.
+// column nx at chunk c xor ((nx >> SWS) mod RC) of the column's dense segment.
 template <int N, bool SSB1>
 __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk, int ry0,
                                           float2 *buf) {
@@ -296,7 +300,7 @@ __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk
     const float2 *zsrc = p.Z + ((size_t)slot * p.Bk + kk) * S::H * N + ry0;
     for (int e = threadIdx.x; e < S::H * S::RC; e += kFusedThreads) {
         const int nx = e / S::RC, c = e - nx * S::RC;
-        const int cd = SSB1 ? (c ^ (nx & (S::RC - 1))) : c;
+        const int cd = SSB1 ? (c ^ ((nx >> S::SWS) & (S::RC - 1))) : c;
         cp_async16(buf + nx * S::LDC + 2 * cd, zsrc + (size_t)nx * N + 2 * c);
     }
     if (SSB1) {
@@ -362,7 +366,8 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
 #pragma unroll
             for (int r = 0; r < kPts; ++r) {
                 const int nx = j + S::T * r;  // element (nx, lr): chunk lr / 2 of column nx, swizzled
-                v[r] = active ? cur[nx * S::LDC + 2 * ((lr >> 1) ^ (nx & (S::RC - 1))) + (lr & 1)]
+                v[r] = active ? cur[nx * S::LDC + 2 * ((lr >> 1) ^ ((nx >> S::SWS) & (S::RC - 1))) +
+                                    (lr & 1)]
                               : make_float2(0.f, 0.f);
             }
             reg_fft<N, kPts, +1>(v, smem + S::OFF_RFFT + grp * S::SMR, twN, j, warp_bar);
