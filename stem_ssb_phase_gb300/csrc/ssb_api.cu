@@ -264,10 +264,12 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     SSB_ALLOC(c->kturn, (size_t)c->n_bf, sb);
     SSB_ALLOC(c->E, P, sb);
     SSB_ALLOC(c->tw, (size_t)N, sb);
-    // Both transfers run on the persistent fused kernel.  Batch size and ring depth:
-    // several short batches in flight keep the column work flowing while slow row tasks
-    // drain the oldest slots, within an L2-sized ring (about 67 MB at N = 512; SSB1
-    // transforms all N columns, so its batches hold half the planes)
+    // Both transfers run on the persistent fused kernel.  Batch size and ring depth: four
+    // batches in flight keep the column work flowing while row tasks drain the oldest
+    // slot, and the ring stays within L2 (67 MB at N = 512; SSB1 transforms all N columns,
+    // so its batches hold half the planes).  Larger batches amortise each row task's fixed
+    // costs further but push the ring out of L2: at 24 planes and more the whole
+    // intermediate round-trips HBM (about 3x the G bytes of DRAM traffic).
     const bool ssb1 = transfer == SSB_TRANSFER_SSB1;
     c->Bk = std::min(ssb1 ? SSB_FUSED_BK / 2 : SSB_FUSED_BK, c->n_bf);
     c->D = SSB_FUSED_RING;
