@@ -287,7 +287,8 @@ def run_ours(args, rank, world, local_rank):
             ach = inst / (ms / nl / 1e3) / 1e12
             pk = sms * 4 * clk["sm_mhz"] * 1e6 / 1e12
             roof_alu = {"bound": "alu", "kernel": name, "achieved": round(ach, 3), "peak": round(pk, 3),
-                        "unit": "Twarp-inst/s", "frac": round(ach / pk, 4),
+                        "unit": "Twarp-inst/s", "frac": round(ach / pk, 4), "traffic": traffic,
+                        "warp_instructions_per_launch": int(inst),
                         "peak_kind": "derived: %d SMs x 4 schedulers x 1 warp-instruction/clock x %.0f MHz sampled"
                                      % (sms, clk["sm_mhz"]),
                         "pipes_pct_of_peak": rec.get("pipes_pct"),
@@ -322,8 +323,11 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": "replicas x%d" % world},
             "e2e": e2e,
             "gpu_launches": int(launches),
-            "roofline": roof,
-            "roofline_alu": roof_alu,
+            # the kernel is bound by instruction issue: its issue-slot roofline is the
+            # primary one whenever ncu counters of these sources exist; the HBM one is
+            # kept beside it (and is primary only without fresh counters)
+            "roofline": roof_alu if roof_alu is not None else roof,
+            "roofline_hbm": roof,
             "hbm_fraction_g_only": round(hbm_g_only / peak, 4),
             "kernel_ms_per_objective": {k: round(v[1], 4) for k, v in prof.items()},
             "clocks": clk,
