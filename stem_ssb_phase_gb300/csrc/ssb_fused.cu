@@ -1,28 +1,31 @@
-// Persistent, ticket-scheduled evaluation of the exact SSB objective (SSB2 transfer).
+// Persistent, ticket-scheduled evaluation of the exact SSB objective, for both transfers.
 //
 // The pages locate the cost of the exact objective in the column -> row intermediate that
 // is written and re-read through global memory ("Later SSB performance checkpoints",
-// 2026-09-11 checkpoints: about 18.8 GB per evaluation).  Here that intermediate never
-// leaves L2: BF planes are processed in batches of Bk planes through a ring of D batch
-// slots (tens of MB, L2-resident), by one persistent kernel on every SM.
+// 2026-09-11 checkpoints: about 18.8 GB per evaluation).  Here that intermediate stays in
+// L2: BF planes are processed in batches of Bk planes through a ring of D batch slots
+// (tens of MB), by one persistent kernel on every SM.
 //
-// Work is cut in half exactly.  Off DC and the Nyquist lines the corrected spectrum is
-// anti-Hermitian, C(-Q) = -conj C(Q) (the relation of "SSB performance notes", 257-row
-// intermediate prototype).  So only the N/2+1 half-plane columns are corrected and
-// column-transformed; each row is rebuilt from them as
+// SSB2 (the normalised two-sideband transfer) does half the work, exactly.  Off DC and
+// the Nyquist lines its corrected spectrum is anti-Hermitian, C(-Q) = -conj C(Q) (the
+// relation of "SSB performance notes", 257-row intermediate prototype).  So only the
+// N/2+1 half-plane columns are corrected and column-transformed; each row is rebuilt from
+// them as
 //     Zfull(ry, N - nx) = -conj Z(ry, nx) + 2 (-1)^ry conj h(nx),   1 <= nx < N/2,
 // where h(nx) = (C(N/2, nx) + conj C(N/2, N - nx)) / 2 is the Hermitian part of the
 // Nyquist row, whose bins have no negative-frequency partner (the violation the pages
 // isolate).  Columns 0 and N/2 are transformed in full.  The result equals the plain
-// two-dimensional inverse transform in exact arithmetic.
+// two-dimensional inverse transform in exact arithmetic.  SSB1 (the literal
+// single-sideband factor) has no such symmetry: all N columns, full complex rows.
 //
 // Tasks (ticket order, phase p = [columns of batch p, rows of batch p-1]):
-//   column task (batch b, plane, CW half-plane columns): G load, correction, column IFFT,
-//       store to the ring slot, one column contiguous, Z[slot][plane][nx][ry]; the task
-//       that completes a plane's column pass also transforms its Nyquist-row term;
-//   row task (batch b, RT rows): for each plane of the batch, rebuild the full rows,
-//       row IFFT, phi = atan2, accumulate; then add the batch's per-pixel sums into the
-//       float64 S1 (and S2, object) in batch order.
+//   column task (batch b, plane, CW columns, kColsPerWarp per warp): G load, correction,
+//       column IFFT, store to the ring slot, one column contiguous, Z[slot][plane][nx][ry];
+//       columns with exactly zero transfer store zeros without the work; for SSB2 the
+//       task that completes a plane's column pass also transforms its Nyquist-row term;
+//   row task (batch b, RT rows): for each plane of the batch, rebuild the full rows (SSB2)
+//       or take them as they are (SSB1), row IFFT, phi = atan2, accumulate; then add the
+//       batch's per-pixel sums into the float64 S1 (and S2, object) in batch order.
 // A block takes its next ticket when its current task has finished its work: a column
 // task just before its completion fence (the round trips overlap), a row task after its
 // signal.  (Taking a column ticket any earlier, even just before the task's ring writes,

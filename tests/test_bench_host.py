@@ -1,6 +1,6 @@
 """Host-side logic of bench.py: the multi-rank reduction on world_size-2 gloo ranks (the
-data path has no collective; only the timing is reduced), and the reference arm's JSON
-line on the tiny workload."""
+data path has no collective; only the timing is reduced), the reference arm's JSON
+line on the tiny workload, and the source digest that keys the ncu counters."""
 import json
 import os
 import socket
@@ -66,3 +66,13 @@ def test_reference_arm_json_line():
         assert key in line, key
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_source_digest_ignores_comments_but_not_code():
+    """The counters' source digest follows the compiled code: comment and layout edits keep
+    it, any code edit (including inside a string literal) changes it."""
+    import bench
+    src = 'int a = 1; // note\n/* block\n comment */ const char *s = "x // y";\n'
+    assert bench._code_only(src) == bench._code_only(src.replace("note", "other").replace("\n", "\n\n"))
+    assert bench._code_only(src) != bench._code_only(src.replace("a = 1", "a = 2"))
+    assert bench._code_only(src) != bench._code_only(src.replace("x // y", "x // z"))
