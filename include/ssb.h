@@ -92,10 +92,12 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
                        int counts_on_device, ssb_transfer transfer, void *cuda_stream,
                        ssb_ctx **out);
 
-/* Exact objective for T trials (page "SSB performance notes", fused multi-candidate
- * evaluation: trials share the G cache reads, each keeps its own correction, FFTs,
- * phase and loss).  theta: host [T]; loss_out: host [T] (float64).  T >= 1.
- * Each entry equals the loss of a single-trial call with the same theta, bit for bit. */
+/* Exact objective for T trials (page "SSB performance notes", multi-candidate
+ * evaluation: each trial keeps its own correction, FFTs, phase and loss).  Here each
+ * trial is one launch of the persistent kernel, which reads the G cache once; the G read
+ * is not what bounds the kernel, so trials do not share it.  theta: host [T]; loss_out:
+ * host [T] (float64).  T >= 1.  Each entry equals the loss of a single-trial call with the
+ * same theta, bit for bit; the transfer is the context's. */
 ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *loss_out,
                           void *cuda_stream);
 

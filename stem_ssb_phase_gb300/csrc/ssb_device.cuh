@@ -1,5 +1,6 @@
 // Device building blocks shared by the SSB kernels: complex helpers, a batched
-// shared-memory Stockham FFT and the per-element SSB correction factor.
+// shared-memory Stockham FFT (G-cache builder), the soft aperture, the per-element SSB2
+// and SSB1 corrections, the zero-transfer column tests and the atan2 used for phases.
 #pragma once
 
 #include <cuda_runtime.h>

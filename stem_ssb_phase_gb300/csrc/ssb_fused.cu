@@ -50,7 +50,7 @@ constexpr int kPts = 16;                    // points per thread in every transf
 #ifndef SSB_COLS_PER_WARP
 #define SSB_COLS_PER_WARP 2
 #endif
-constexpr int kColsPerWarp = SSB_COLS_PER_WARP;  // half-plane columns per warp-group in a task
+constexpr int kColsPerWarp = SSB_COLS_PER_WARP;  // columns each transform group takes per task
 constexpr unsigned kWaitLimit = 1u << 24;  // polls of ~0.1-1 us each before giving up
 
 struct FusedParams {
