@@ -93,13 +93,8 @@ __device__ int fft_batch_smem(float2 *buf0, float2 *buf1, int NF, int LD, const 
 // Per-trial constants of the correction (float32 copies of host float64 values).
 struct TrialConst {
     float cr, sr;       // cos, sin of the scan rotation
-    float lam;          // wavelength (Angstrom)
-    float inv_nstep;    // 1 / (N * scan step)  (1/Angstrom per frequency bin)
     float semi;         // aperture semiangle (rad)
     float inv_dalpha;   // 1 / detector sampling (1/rad)
-    int mode;           // 0 = SSB2, 1 = SSB1
-    // lambda Q' = (lxs sx + lxy sy, lys sx + lyy sy) for signed bins (sx, sy)
-    float lxs, lxy, lys, lyy;
     float inner2;       // |alpha|^2 at or below which a(alpha) = 1 (negative: never)
     float outer2;       // |alpha|^2 at or above which a(alpha) = 0
     float lam_q;        // lambda / (N * scan step): |lambda Q'| per frequency bin (rad)
@@ -141,6 +136,27 @@ __device__ __forceinline__ float aperture_r2(float r2, const TrialConst &tc) {
     return a < kApertureFloor ? 0.0f : a;
 }
 
+
+// Squared distances |alpha_k -+ lambda Q'|^2 along one scan-frequency column sx, without
+// forming lambda Q': with (u, w) = alpha_k in the frame rotated by the scan rotation and
+// q = lam_q, |alpha_k -+ lambda Q'|^2 = |alpha_k|^2 + q^2 (sx^2 + sy^2) -+ 2 q (u sx + w sy).
+// The caller fills base = |alpha_k|^2 + q^2 sx^2, p0 = q u sx, qw = q w and q2 = q^2 once
+// per column; each element then costs five float operations.
+struct ColGeom {
+    float base, p0, qw, q2;
+};
+
+__device__ __forceinline__ ColGeom col_geom(int sx, float ax, float ay, const TrialConst &tc) {
+    const float q = tc.lam_q, fsx = (float)sx;
+    const float u = fmaf(ax, tc.cr, ay * tc.sr), w = fmaf(ay, tc.cr, -ax * tc.sr);
+    ColGeom cg;
+    cg.q2 = q * q;
+    cg.base = fmaf(cg.q2, fsx * fsx, fmaf(ax, ax, ay * ay));
+    cg.p0 = q * u * fsx;
+    cg.qw = q * w;
+    return cg;
+}
+
 // SSB2 correction of one G value at signed bins (sx, sy): C = G conj(Gamma)/|Gamma|, 0 where
 // Gamma = 0.  With chi quadratic, chi(alpha_k -+ lambda Q') = chi(alpha_k) + chi(lambda Q')
 // -+ B with B = 2 pi alpha_k^T M Q' linear in Q (M the aberration matrix), so
@@ -149,16 +165,16 @@ __device__ __forceinline__ float aperture_r2(float r2, const TrialConst &tc) {
 // and conj(Gamma)/|Gamma| = e^{iB} conj(D)/|D| (an exact rewriting).  chiQ comes from the
 // per-trial table E = e^{i chiQ}; B is carried exactly as a 32-bit fixed-point fraction of
 // a turn, b_x sx + b_y sy mod 2^32, so its range reduction is exact.  The per-column terms
-// are hoisted by the caller: lx0 = lxs sx, ly0 = lys sx, phx = b_x sx; DC (C(0) = G(0))
-// and a_k = 0 are handled there too.
-__device__ __forceinline__ float2 correct_ssb2(float2 g, int sy, float2 e, float gx, float gy,
-                                               uint32_t phx, uint32_t by, float lx0, float ly0,
-                                               const TrialConst &tc) {
-    const float fsy = (float)sy;
-    const float lx = fmaf(tc.lxy, fsy, lx0), ly = fmaf(tc.lyy, fsy, ly0);
-    const float dmx = gx - lx, dmy = gy - ly, dpx = gx + lx, dpy = gy + ly;
-    const float am = aperture_r2(fmaf(dmx, dmx, dmy * dmy), tc);
-    const float ap = aperture_r2(fmaf(dpx, dpx, dpy * dpy), tc);
+// come from the caller: the column geometry cg and phx = b_x sx; fsy is the signed bin sy
+// as a float, sy itself enters the exact turn-fraction phase; DC (C(0) = G(0)) and
+// a_k = 0 are handled there too.
+__device__ __forceinline__ float2 correct_ssb2(float2 g, float fsy, int sy, float2 e,
+                                                const ColGeom &cg, uint32_t phx, uint32_t by,
+                                                const TrialConst &tc) {
+    const float b = fmaf(cg.q2, fsy * fsy, cg.base);
+    const float pq = fmaf(cg.qw, fsy, cg.p0);
+    const float am = aperture_r2(fmaf(-2.0f, pq, b), tc);
+    const float ap = aperture_r2(fmaf(2.0f, pq, b), tc);
     const float dx = (am - ap) * e.x, dy = (am + ap) * e.y;
     const float d2 = fmaf(dx, dx, dy * dy);
     if (!(d2 > 0.0f)) return make_float2(0.0f, 0.0f);  // zero transfer
@@ -171,19 +187,19 @@ __device__ __forceinline__ float2 correct_ssb2(float2 g, int sy, float2 e, float
 
 // SSB1 correction of one G value, F = e^{iB} conj(E) where a(alpha_k - lambda Q') > 0 and 0
 // elsewhere (the caller handles DC and a_k = 0): chi(alpha_k) - chi(alpha_k - lambda Q') =
-// B - chi(lambda Q'), the same separable terms as correct_ssb2.
-__device__ __forceinline__ float2 correct_ssb1(float2 g, int sy, float2 e, float gx, float gy,
-                                               uint32_t phx, uint32_t by, float lx0, float ly0,
-                                               const TrialConst &tc) {
-    const float fsy = (float)sy;
-    const float lx = fmaf(tc.lxy, fsy, lx0), ly = fmaf(tc.lyy, fsy, ly0);
-    const float dmx = gx - lx, dmy = gy - ly;
-    if (!(aperture_r2(fmaf(dmx, dmx, dmy * dmy), tc) > 0.0f)) return make_float2(0.0f, 0.0f);
+// B - chi(lambda Q'), the same separable terms as the SSB2 correction.
+__device__ __forceinline__ float2 correct_ssb1(float2 g, float fsy, int sy, float2 e,
+                                                const ColGeom &cg, uint32_t phx, uint32_t by,
+                                                const TrialConst &tc) {
+    const float b = fmaf(cg.q2, fsy * fsy, cg.base);
+    const float pq = fmaf(cg.qw, fsy, cg.p0);
+    if (!(aperture_r2(fmaf(-2.0f, pq, b), tc) > 0.0f)) return make_float2(0.0f, 0.0f);
     const uint32_t ph = phx + by * (uint32_t)sy;
     float sb, cb;
     __sincosf((float)(int32_t)ph * 1.4629180792671596e-09f, &sb, &cb);  // 2 pi ph / 2^32
     return cmul(g, cmul(make_float2(cb, sb), cconj(e)));
 }
+
 
 // Phase atan2(y, x) in (-pi, pi]: octant reduction to a = min/max in [0, 1], an odd
 // degree-15 polynomial in a fitted to atan on [0, 1] for this library (float32 Horner

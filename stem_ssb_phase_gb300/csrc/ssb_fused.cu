@@ -243,25 +243,32 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
             }
 #pragma unroll
             for (int r = 0; r < kPts; ++r) ev[r] = __ldg(e + S::T * r);
-            const float lx0 = p.tc.lxs * (float)sx, ly0 = p.tc.lys * (float)sx;
+            const ColGeom cg = col_geom(sx, geo.x, geo.y, p.tc);
+            const float fj = (float)j;
             const uint32_t phx = bt.x * (uint32_t)sx;
             const bool active = geo.z > 0.0f;  // a(alpha_k) = 0: only the DC term survives
 #pragma unroll
             for (int r = 0; r < kPts; ++r) {
                 const int ny = j + S::T * r;
-                const int sy = ny < N / 2 ? ny : ny - N;
+                // signed bin: ny for r < kPts/2 (ny < N/2), ny - N above
+                const int off = S::T * r - (r >= kPts / 2 ? N : 0);
+                const int sy = j + off;
+                const float fsy = fj + (float)off;
                 const float2 gv = v[r];
                 float2 cv = make_float2(0.f, 0.f);
                 if (active)
-                    cv = SSB1 ? correct_ssb1(gv, sy, ev[r], geo.x, geo.y, phx, bt.y, lx0, ly0, p.tc)
-                              : correct_ssb2(gv, sy, ev[r], geo.x, geo.y, phx, bt.y, lx0, ly0, p.tc);
+                    cv = SSB1 ? correct_ssb1(gv, fsy, sy, ev[r], cg, phx, bt.y, p.tc)
+                              : correct_ssb2(gv, fsy, sy, ev[r], cg, phx, bt.y, p.tc);
                 if ((nx | ny) == 0) cv = gv;  // C(0) = G(0)
                 if (!SSB1 && r == kPts / 2 && j == 0 && nx >= 1 && nx < N / 2) {
                     // Nyquist row (ny = N/2): the mirror bin N - nx has no partner and
-                    // carries its own correction, at signed bins (-nx, -N/2)
+                    // carries its own correction, at signed bins (-nx, -N/2), where the
+                    // column geometry has p0 negated
                     const float2 em = __ldg(p.Et + (size_t)(N - nx) * N + N / 2);
-                    const float2 c2 = active ? correct_ssb2(cconj(gv), -N / 2, em, geo.x, geo.y,
-                                                            0u - phx, bt.y, -lx0, -ly0, p.tc)
+                    ColGeom cm = cg;
+                    cm.p0 = -cg.p0;
+                    const float2 c2 = active ? correct_ssb2(cconj(gv), -(float)(N / 2), -N / 2, em, cm,
+                                                             0u - phx, bt.y, p.tc)
                                              : make_float2(0.f, 0.f);
                     hval = make_float2(0.5f * (cv.x + c2.x), 0.5f * (cv.y - c2.y));
                     hstore = true;

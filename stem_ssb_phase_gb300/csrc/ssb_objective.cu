@@ -80,16 +80,9 @@ TrialConst make_trial_const(const ObjectiveArgs &a, const TrialHost &th, int N) 
     TrialConst tc;
     tc.cr = (float)th.cr;
     tc.sr = (float)th.sr;
-    tc.lam = (float)a.lam;
-    tc.inv_nstep = (float)(1.0 / (N * a.step));
     tc.semi = (float)a.semi;
     tc.inv_dalpha = (float)(1.0 / a.dalpha);
-    tc.mode = a.mode;
     const double q = a.lam / (N * a.step);
-    tc.lxs = (float)(q * th.cr);
-    tc.lxy = (float)(-q * th.sr);
-    tc.lys = (float)(q * th.sr);
-    tc.lyy = (float)(q * th.cr);
     const double inner = a.semi - 0.5 * a.dalpha, outer = a.semi + 0.5 * a.dalpha;
     tc.inner2 = inner > 0.0 ? (float)(inner * inner) * (1.0f - 4e-7f) : -1.0f;
     tc.outer2 = (float)(outer * outer) * (1.0f + 4e-7f);
