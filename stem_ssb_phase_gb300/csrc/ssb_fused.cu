@@ -34,6 +34,11 @@
 // Every wait is bounded; on timeout the kernel raises an error flag, all waits stop and
 // the host reports SSB_ERR_TIMEOUT.
 #include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>           // CUtensorMap (the encode call is resolved at run time)
+#include <cudaTypedefs.h>
 
 #include "ssb_device.cuh"
 #include "ssb_internal.h"
@@ -96,6 +101,12 @@ struct FusedShape {
     // chunks allow).
     static constexpr int LDC = SSB1 ? RT : RT + 2;
     static constexpr int SWS = RT == 8 ? 1 : 0;
+    // SSB1 with 8- or 16-row segments stages each plane with 2D tensor copies whose 64- or
+    // 128-byte swizzle is exactly the chunk xor above (16-byte chunk bits 4.. of the shared
+    // address xor bits 7..); boxes of BOXN columns.  Other shapes use cp.async.
+    static constexpr bool TMA = SSB1 && (RT == 8 || RT == 16);
+    static constexpr int BOXN = H < 256 ? H : 256;
+    static constexpr int NBOX = (H + BOXN - 1) / BOXN;
     // dynamic shared memory layout, in float2 units.  A block runs one task at a time, so
     // the column task's FFT scratch and the row task's scratch + staged planes share OFF_U.
     static constexpr int SMR = RegFFT<M, RE>::SMEM;                 // row FFT scratch per group
@@ -105,11 +116,14 @@ struct FusedShape {
     static constexpr int OFF_U = OFF_RED + 16;
     static constexpr int OFF_FFT = OFF_U;                           // column task: [GROUPS][SMF]
     static constexpr int OFF_RFFT = OFF_U;                          // row task: [GROUPS][SMR]
-    static constexpr int OFF_TILE = OFF_RFFT + (GROUPS * SMR + 1) / 2 * 2;  // [2][TILEBUF]
+    // [2][TILEBUF]; tensor-copy destinations start on a 1024-byte boundary (128 float2)
+    static constexpr int OFF_TILE = TMA ? (OFF_RFFT + GROUPS * SMR + 127) / 128 * 128
+                                        : OFF_RFFT + (GROUPS * SMR + 1) / 2 * 2;
     static constexpr int TILEBUF = SSB1 ? H * LDC : H * LDC + LDZ + M;  // segments (, h, Rp)
     static constexpr int U_COL = GROUPS * SMF;
     static constexpr int U_ROW = OFF_TILE - OFF_U + 2 * TILEBUF;
-    static constexpr int TOTAL = OFF_U + (U_COL > U_ROW ? U_COL : U_ROW);
+    // + 128 float2 so that the tiles can be placed on a 1024-byte boundary at run time
+    static constexpr int TOTAL = OFF_U + (U_COL > U_ROW ? U_COL : U_ROW) + (TMA ? 128 : 0);
     static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float2);
 };
 
@@ -126,6 +140,34 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int K>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory"); }
+
+// mbarrier and tensor-copy helpers (shared addresses from __cvta_generic_to_shared).
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+    asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0u;
+}
+// One 2D box of the tensor map into shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
+}
 
 __device__ __forceinline__ void red_relaxed_add(unsigned *p, unsigned v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -158,6 +200,17 @@ __device__ bool wait_at_least(const unsigned *addr, unsigned target, unsigned *e
         __nanosleep(128);
     }
     return true;
+}
+
+// Wait until the barrier's phase with the given parity has completed.  Bounded: it gives
+// up when the error flag is raised elsewhere, or raises it when the poll budget runs out.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err) {
+    for (unsigned polls = 0; polls < kWaitLimit; ++polls) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((polls & 255u) == 255u && ld_acquire(err) != 0u) return false;
+    }
+    atomicOr(err, 4u);
+    return false;
 }
 
 // Transforms never span warps (T <= 32), so their exchanges need only warp sync.
@@ -326,6 +379,22 @@ __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk
     cp_async_commit();
 }
 
+// Tensor-copy staging of one SSB1 plane (one thread): NBOX boxes of BOXN columns x RT rows
+// of the ring, swizzled by the copy itself, completing on bar.
+template <int N, bool SSB1>
+__device__ __forceinline__ void row_issue_tma(const FusedParams &p, const CUtensorMap *map,
+                                              int slot, int kk, int ry0, float2 *buf,
+                                              uint32_t bar) {
+    using S = FusedShape<N, SSB1>;
+    // the buffer was last used through ordinary loads and stores
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(bar, (unsigned)(S::TILEBUF * sizeof(float2)));
+    const int row0 = (slot * p.Bk + kk) * S::H;
+#pragma unroll
+    for (int bx = 0; bx < S::NBOX; ++bx)
+        tma_load_2d(smem_u32(buf + bx * S::BOXN * S::RT), map, ry0, row0 + bx * S::BOXN, bar);
+}
+
 // Row ry of the corrected image, split by symmetry (exact):
 //   Im c = real IFFT of Y(m) = -i (Z(m) - s h(m)) (0 < m < N/2), Y(0) = Im Z(0),
 //          Y(N/2) = Im Z(N/2), done as one N/2-point complex IFFT of
@@ -333,9 +402,12 @@ __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk
 //          whose output holds Im c at pixels 2j (real part) and 2j+1 (imaginary part);
 //   Re c = Re Z(0) + (-1)^rx Re Z(N/2) + s Rp(rx),   s = (-1)^ry.
 // SSB1 row ry: one N-point complex IFFT of the staged row, c at pixels j + T r.
+// With tensor-copy staging (S::TMA), bars holds the two tile buffers' barriers and tphase
+// their completed-phase parities (bit i for buffer i), the same in every thread.
 template <int N, bool OBJ, bool SSB1>
 __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int planes,
-                         unsigned *plane_free, unsigned *chain, unsigned *err, int *s_ok) {
+                         unsigned *plane_free, unsigned *chain, unsigned *err, int *s_ok,
+                         const CUtensorMap *map, uint32_t bars, unsigned &tphase) {
     using S = FusedShape<N, SSB1>;
     const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
     const int slot = b % p.D;
@@ -346,6 +418,9 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
     const float sg = (ry & 1) ? -1.0f : 1.0f;       // (-1)^ry
     const float2 *twN = smem + S::OFF_TW;
     float2 *tiles = smem + S::OFF_TILE;
+    if (S::TMA)  // tensor-copy destinations on a 1024-byte boundary (slack reserved in TOTAL)
+        tiles = reinterpret_cast<float2 *>((reinterpret_cast<uintptr_t>(tiles) + 1023) &
+                                           ~(uintptr_t)1023);
     float acc1[2 * 8];
     float2 acco[2 * 8];
     float acc2 = 0.f;
@@ -354,17 +429,30 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         acc1[r] = 0.f;
         acco[r] = make_float2(0.f, 0.f);
     }
-    row_issue<N, SSB1>(p, slot, 0, ry0, tiles);
+    if (S::TMA) {
+        if (tid == 0) row_issue_tma<N, SSB1>(p, map, slot, 0, ry0, tiles, bars);
+    } else {
+        row_issue<N, SSB1>(p, slot, 0, ry0, tiles);
+    }
     for (int kk = 0; kk < planes; ++kk) {
-        float2 *cur = tiles + (kk & 1) * S::TILEBUF;
+        const int buf = kk & 1;
+        float2 *cur = tiles + buf * S::TILEBUF;
         __syncthreads();  // everyone is done with the other buffer (plane kk - 1)
-        if (kk + 1 < planes) {
-            row_issue<N, SSB1>(p, slot, kk + 1, ry0, tiles + ((kk + 1) & 1) * S::TILEBUF);
-            cp_async_wait<1>();
+        if (S::TMA) {
+            if (tid == 0 && kk + 1 < planes)
+                row_issue_tma<N, SSB1>(p, map, slot, kk + 1, ry0, tiles + (buf ^ 1) * S::TILEBUF,
+                                       bars + 8u * (buf ^ 1));
+            mbar_wait(bars + 8u * buf, (tphase >> buf) & 1u, err);  // plane kk has landed
+            tphase ^= 1u << buf;
         } else {
-            cp_async_wait<0>();
+            if (kk + 1 < planes) {
+                row_issue<N, SSB1>(p, slot, kk + 1, ry0, tiles + (buf ^ 1) * S::TILEBUF);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();  // plane kk has landed for every thread
         }
-        __syncthreads();  // plane kk has landed for every thread
         if (tid == 0) {
             // This task no longer needs plane kk of the slot: columns of batch b + D may
             // overwrite it once every row task has passed it.  The plane's reads have all
@@ -544,13 +632,22 @@ __device__ Task decode_ticket(const FusedParams &p, unsigned t) {
 }
 
 template <int N, bool OBJ, bool SSB1>
-__global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(FusedParams p) {
+__global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
+    k_fused(FusedParams p, const __grid_constant__ CUtensorMap ring_map) {
     using S = FusedShape<N, SSB1>;
     extern __shared__ __align__(16) float2 smem[];
     __shared__ unsigned s_ticket;
     __shared__ int s_ok;
     __shared__ int s_nyq;
+    __shared__ __align__(8) unsigned long long s_tile_bar[2];  // tensor-copy tile barriers
     const int tid = threadIdx.x;
+    const uint32_t tile_bars = smem_u32(s_tile_bar);
+    unsigned tile_phase = 0u;
+    if (S::TMA && tid == 0) {
+        mbar_init(tile_bars, 1u);
+        mbar_init(tile_bars + 8u, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     for (int i = tid; i < N; i += kFusedThreads) smem[S::OFF_TW + lay(i)] = p.tw[i];
     for (int i = tid; i < S::M; i += kFusedThreads) smem[S::OFF_TW2 + lay(i)] = p.tw[2 * i];
     unsigned *ticket = p.sync;
@@ -608,7 +705,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM) k_fused(Fuse
             __syncthreads();
             if (s_ok) {
                 row_task<N, OBJ, SSB1>(p, smem, task.b, task.idx, planes_in(p, task.b), plane_free,
-                                       chain, err, &s_ok);
+                                       chain, err, &s_ok, &ring_map, tile_bars, tile_phase);
             } else if (tid == 0) {  // release the planes anyway so that no wait is left behind
                 for (int kk = 0; kk < planes_in(p, task.b); ++kk)
                     atomicAdd(plane_free + (size_t)task.b * p.Bk + kk, 1u);
@@ -665,10 +762,49 @@ size_t fused_hring_elems(int N, int Bk, int D) { return (size_t)D * Bk * ldz_for
 size_t fused_rring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)(N / 2); }
 int fused_row_tasks(int N) { return row_tasks_for(N); }
 
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link against the driver
+// library); null if the driver does not provide it.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// The ring as a 2D tensor of 8-byte elements: x = row ry (N, contiguous), y = transformed
+// column of every slot and plane (D Bk H).  Boxes of RT rows x BOXN columns, swizzled to
+// match the row task's reads.
+template <int N, bool SSB1>
+static cudaError_t ring_tensor_map(const FusedParams &fp, CUtensorMap *map) {
+    using S = FusedShape<N, SSB1>;
+    std::memset(map, 0, sizeof(*map));
+    if (!S::TMA) return cudaSuccess;  // not used
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)fp.D * fp.Bk * S::H};
+    const cuuint64_t strides[1] = {(cuuint64_t)N * sizeof(float2)};
+    const cuuint32_t box[2] = {(cuuint32_t)S::RT, (cuuint32_t)S::BOXN};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 2, fp.Z, dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              S::RT == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int N, bool OBJ, bool SSB1>
 static cudaError_t fused_launch(const FusedParams &fp, cudaStream_t s) {
     using S = FusedShape<N, SSB1>;
     cudaError_t e;
+    CUtensorMap ring_map;
+    if ((e = ring_tensor_map<N, SSB1>(fp, &ring_map)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_fused<N, OBJ, SSB1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)S::BYTES)) != cudaSuccess)
         return e;
@@ -682,7 +818,7 @@ static cudaError_t fused_launch(const FusedParams &fp, cudaStream_t s) {
     const long tickets = (long)fp.nbatch * (fp.Bk * S::CT + S::NR);
     const int grid = (int)std::max(1L, std::min((long)sms * std::max(per_sm, 1), tickets));
     prof_begin("k_fused", s);
-    k_fused<N, OBJ, SSB1><<<grid, kFusedThreads, S::BYTES, s>>>(fp);
+    k_fused<N, OBJ, SSB1><<<grid, kFusedThreads, S::BYTES, s>>>(fp, ring_map);
     prof_end(s);
     count_launch();
     return cudaGetLastError();
