@@ -7,5 +7,5 @@ from .ssb_oracle import (  # noqa: F401
     MODES, Geom, aperture, chi, probe, scan_frequencies, rotated_frequencies,
     dft_matrix, fft2_forward, ifft2_inverse, g_plane, full_plane, transfer,
     corrected_spectrum, bf_phase, objective, loss_batch, object_from_spectrum_sum,
-    branch_cut_pixels, default_workers,
+    upsample_object, branch_cut_pixels, default_workers,
 )

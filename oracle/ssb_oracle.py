@@ -29,7 +29,8 @@ For every bright-field (BF) detector pixel k, in row-major detector order,
 Outputs: loss L = (1/P) sum_r [S2/n_bf - (S1/n_bf)^2] (population variance over the
 BF terms averaged over all scan pixels; every BF pixel stays in the normalisation,
 "SSB performance notes", automatic 8,937-BF checkpoint), mean phase S1/n_bf, and
-the object redraw O(r) = (1/n_bf) sum_k c_k(r) with its phase ("phase-of-mean").
+the object redraw O(r) = (1/n_bf) sum_k c_k(r) with its phase ("phase-of-mean"), and its
+band-limited interpolation onto a finer scan grid (upsample_object).
 
 Readings where the pages are silent (each listed in the design notes):
   * transfer "ssb2" (default) is Gamma above; "ssb1" is the single-sideband factor
@@ -319,6 +320,26 @@ def object_from_spectrum_sum(geom, theta, counts, mode="ssb2"):
     for k in range(g.n_bf):
         csum += corrected_spectrum(g, k, full_plane(g_plane(counts[k])), theta, mode)
     return np.fft.ifft2(csum) / g.n_bf
+
+
+def upsample_object(obj: np.ndarray, factor: int) -> np.ndarray:
+    """Band-limited interpolation of the object redraw onto a scan grid `factor` times
+    finer, the plainest reading of the pages' reconstruct(result, upsample=factor)
+    ("Later SSB performance checkpoints", joint CUDA calibration, output reconstruction
+    at factors 1-4): the N x N spectrum of the object keeps its fftfreq (signed, Nyquist
+    negative) frequencies on the (factor N)^2 grid, every other frequency is zero, and
+    the inverse transform is scaled so that the samples at multiples of `factor` are the
+    original ones:
+        O_up(m) = (1/N^2) sum_k O^(k) exp(2 pi i k.m / (factor N)).
+    """
+    n = obj.shape[0]
+    assert obj.shape == (n, n) and factor >= 1
+    fn = factor * n
+    spec = np.fft.fft2(np.asarray(obj, dtype=np.complex128))
+    k = np.fft.fftfreq(n, d=1.0 / n).astype(np.int64)  # signed integer frequencies
+    big = np.zeros((fn, fn), dtype=np.complex128)
+    big[np.ix_(k % fn, k % fn)] = spec
+    return np.fft.ifft2(big) * factor * factor
 
 
 def branch_cut_pixels(phases: np.ndarray, tol: float = 1e-4) -> np.ndarray:

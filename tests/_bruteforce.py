@@ -93,3 +93,28 @@ def objective_loops(counts, geom, theta, mode="ssb2"):
             m = s1[y][x] / nb
             loss += s2[y][x] / nb - m * m
     return loss / p, phases
+
+
+def upsample_loops(obj, factor):
+    """Band-limited interpolation by direct double sums (forward DFT over the N x N grid at
+    signed frequencies, then the inverse sum evaluated on the (factor N)^2 grid), per-point
+    cmath; tiny inputs only."""
+    n = len(obj)
+    fn = factor * n
+    ks = [_signed(q, n) for q in range(n)]
+    spec = {}
+    for ky in ks:
+        for kx in ks:
+            acc = 0j
+            for ny in range(n):
+                for nx in range(n):
+                    acc += obj[ny][nx] * cmath.exp(-2j * math.pi * (ky * ny + kx * nx) / n)
+            spec[(ky, kx)] = acc
+    out = [[0j] * fn for _ in range(fn)]
+    for my in range(fn):
+        for mx in range(fn):
+            acc = 0j
+            for (ky, kx), v in spec.items():
+                acc += v * cmath.exp(2j * math.pi * (ky * my + kx * mx) / fn)
+            out[my][mx] = acc / (n * n)
+    return out

@@ -302,3 +302,54 @@ def test_generator_dose_and_determinism():
     assert np.array_equal(c1, c2)
     assert c1.dtype == np.uint16
     assert abs(c1.mean() / w.mean_count - 1) < 0.01
+
+
+# ---------------------------------------------------------------- upsampled redraw
+
+def _random_object(n, seed):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((n, n)) + 1j * rng.standard_normal((n, n))
+
+
+def test_upsample_factor_one_is_the_identity():
+    obj = _random_object(16, 1)
+    assert np.allclose(oracle.upsample_object(obj, 1), obj, atol=1e-13, rtol=0)
+
+
+@pytest.mark.parametrize("factor", [2, 3, 4])
+def test_upsample_keeps_the_original_samples(factor):
+    """Band-limited interpolation passes through the original samples, whatever the
+    placement of the Nyquist bin."""
+    obj = _random_object(32, factor)
+    up = oracle.upsample_object(obj, factor)
+    assert up.shape == (32 * factor, 32 * factor)
+    assert np.allclose(up[::factor, ::factor], obj, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("a,b", [(3, -5), (-7, 2), (0, 6)])
+def test_upsample_of_a_tone_is_the_continuous_exponential(a, b):
+    """A single in-band frequency interpolates to the exponential itself (closed form):
+    catches a wrong sign, a swapped axis or a frequency placed in the wrong bin."""
+    n, f = 16, 3
+    y, x = np.mgrid[0:n, 0:n]
+    obj = np.exp(2j * np.pi * (a * y + b * x) / n)
+    ym, xm = np.mgrid[0:f * n, 0:f * n]
+    exact = np.exp(2j * np.pi * (a * ym + b * xm) / (f * n))
+    assert np.allclose(oracle.upsample_object(obj, f), exact, atol=1e-12, rtol=0)
+
+
+def test_upsample_matches_direct_sums():
+    from _bruteforce import upsample_loops
+    obj = _random_object(6, 7)
+    ref = np.array(upsample_loops(obj.tolist(), 3))
+    assert np.allclose(oracle.upsample_object(obj, 3), ref, atol=1e-11, rtol=0)
+
+
+def test_upsample_is_band_limited():
+    n, f = 16, 4
+    up = oracle.upsample_object(_random_object(n, 3), f)
+    spec = np.fft.fft2(up)
+    k = np.fft.fftfreq(f * n, d=1.0 / (f * n))
+    inband = (k >= -n // 2) & (k < n // 2)
+    outside = ~np.outer(inband, inband)
+    assert np.abs(spec[outside]).max() < 1e-9 * np.abs(spec).max()
