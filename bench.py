@@ -418,6 +418,79 @@ def run_fit(args):
     ctx.close()
 
 
+def fp32_alu_peak_tflops(sm_mhz: float, sms: int = 152) -> float:
+    """FP32 FMA issue peak on the CUDA cores: 128 lanes per SM, 2 flops per FMA."""
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def upsample_flops(n: int, factor: int) -> float:
+    """Real flops of the two complex interpolation products T = O A^T (N x fN x N) and
+    O_up = A T (fN x fN x N), 8 per complex multiply-add."""
+    fn = factor * n
+    return 8.0 * (n * n * fn + fn * fn * n)
+
+
+def run_upsample(args):
+    """Upsampled object redraw at the benchmark trial: one objective with the object
+    accumulated, then the band-limited interpolation onto the factor-times finer grid.
+    Reports the whole call per redraw (device events around the C-ABI call, output
+    resident on the device) and, from the per-launch profiler, the two interpolation
+    kernels against the FP32 issue peak of the CUDA cores."""
+    import torch
+
+    import stem_ssb_phase_gb300 as ssbgpu
+    from stem_ssb_phase_gb300 import build as _build
+    _build.build()
+    w = ssb_synth.WORKLOADS[args.workload]
+    geom, counts, _ = ssb_synth.simulate_counts_torch(w, "cuda")
+    ctx = ssbgpu.SSB(geom, counts, transfer=args.transfer)
+    del counts
+    torch.cuda.empty_cache()
+    f = args.upsample
+    n = geom.scan_n
+    theta = ssb_synth.draw_trials(w, 1)[0]
+    for _ in range(args.warmup):
+        ctx.reconstruct_upsampled(theta, f)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    l0 = ssbgpu.kernel_launches()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for _ in range(args.steps):
+        ph, obj, loss = ctx.reconstruct_upsampled(theta, f)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    launches = ssbgpu.kernel_launches() - l0
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    prof = {}
+    for _ in range(args.steps):
+        for k, (c, t) in ctx.profile_upsampled(theta, f).items():
+            a = prof.setdefault(k, [0, 0.0])
+            a[0] += c
+            a[1] += t
+    clk = clocks.stop()
+    up_ms = sum(t for k, (c, t) in prof.items() if k.startswith("k_upsample")) / args.steps
+    sm_mhz = clk["sm_mhz"] if clk else 2070.0
+    peak = fp32_alu_peak_tflops(sm_mhz)
+    achieved = upsample_flops(n, f) / (up_ms * 1e-3) / 1e12
+    out = {"metric": "upsampled object redraw (objective + band-limited interpolation), ms per redraw",
+           "value": ms, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": "%s: %dx%d scan, %d BF" % (w.name, n, n, geom.n_bf),
+                      "upsample": f, "output": "%dx%d phase + complex64 object" % (f * n, f * n),
+                      "transfer": args.transfer},
+           "kernels_ms_per_redraw": {k: t / args.steps for k, (c, t) in sorted(prof.items())},
+           "upsample_ms": up_ms,
+           "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "traffic": None,
+                        "peak_basis": "FP32 FMA issue, 152 SMs x 128 lanes x 2 at the median SM clock"},
+           "gpu_launches": launches, "clocks": clk, "loss": loss}
+    print(json.dumps(out), flush=True)
+    ctx.close()
+
+
 def run_reference(args, rank, world):
     """The float64 CPU oracle on a bounded BF sample of the same workload."""
     if rank != 0:
@@ -469,6 +542,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fit", action="store_true",
                     help="time the full fit workload (200 trials + Nelder-Mead + redraw) instead")
+    ap.add_argument("--upsample", type=int, default=0,
+                    help="time the upsampled object redraw at this factor (1-8) instead")
     ap.add_argument("--bf-subset", type=int, default=0,
                     help="evenly spaced BF pixels of the workload (profiling a small case)")
     args = ap.parse_args()
@@ -488,6 +563,9 @@ def main():
         if args.fit:
             if rank == 0:
                 run_fit(args)
+        elif args.upsample and args.impl == "ours":
+            if rank == 0:
+                run_upsample(args)
         elif args.impl == "reference":
             run_reference(args, rank, world)
         else:

@@ -109,6 +109,25 @@ ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *lo
 ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phase_out,
                            float *object_c64_out, double *loss_out, void *cuda_stream);
 
+/* Largest factor ssb_reconstruct_upsampled accepts. */
+#define SSB_MAX_UPSAMPLE 8
+
+/* Object redraw on a scan grid `factor` times finer (page "Later SSB performance
+ * checkpoints", joint CUDA calibration: reconstruction with an upsampling factor of 1 to 4).
+ * The BF-summed object of ssb_reconstruct is interpolated band-limited: its N x N discrete
+ * spectrum is kept at the signed frequencies -N/2 .. N/2-1 of the (factor N)^2 grid, every
+ * other frequency is zero, and the grid's inverse transform is scaled by factor^2 so that
+ * the original samples are kept (O_up[factor m][factor n] = O[m][n]).
+ *   factor:         1 .. SSB_MAX_UPSAMPLE (1 gives the object of ssb_reconstruct)
+ *   phase_out:      device [factor N][factor N] float32, arg of the object  (required)
+ *   object_c64_out: device [factor N][factor N] complex64 interleaved        (nullable)
+ *   loss_out:       host, one float64                                        (nullable)
+ * The context allocates an interpolation table and an N x factor N complex64 intermediate
+ * on the first call with a new factor (not counted by ssb_info); SSB_ERR_OOM if that fails. */
+ssb_status ssb_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int factor,
+                                     float *phase_out, float *object_c64_out, double *loss_out,
+                                     void *cuda_stream);
+
 /* Sizes of the G cache and of the scratch the context holds (either pointer nullable). */
 ssb_status ssb_info(const ssb_ctx *c, size_t *g_bytes, size_t *scratch_bytes);
 
@@ -134,6 +153,13 @@ typedef struct {
 
 ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel_time *out,
                                  int cap, int *n_out, void *cuda_stream);
+
+/* The same per-kernel timing for one ssb_reconstruct_upsampled call (objective, then the
+ * two interpolation products): phase_out as there (device [factor N][factor N] float32);
+ * errors as there.  Synchronises the stream. */
+ssb_status ssb_profile_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int factor,
+                                             float *phase_out, ssb_kernel_time *out, int cap,
+                                             int *n_out, void *cuda_stream);
 
 /* Loss of one trial without any device allocation.  (The pages have no counterpart: this
  * entry point exists for callers of this library that cannot allocate device memory when

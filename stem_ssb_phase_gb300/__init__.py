@@ -21,8 +21,10 @@ STATUS = {0: "SSB_OK", 1: "SSB_ERR_ARG", 2: "SSB_ERR_UNSUPPORTED", 3: "SSB_ERR_O
           4: "SSB_ERR_CUDA", 5: "SSB_ERR_TIMEOUT", 6: "SSB_ERR_DEVICE_FLAG"}
 
 # every symbol include/ssb.h declares
-EXPORTS = ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_info", "ssb_export_g",
-           "ssb_unpack_counts", "ssb_profile_objective", "ssb_loss_noalloc", "ssb_status_string",
+EXPORTS = ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_reconstruct_upsampled",
+           "ssb_info", "ssb_export_g",
+           "ssb_unpack_counts", "ssb_profile_objective", "ssb_profile_reconstruct_upsampled",
+           "ssb_loss_noalloc", "ssb_status_string",
            "ssb_last_error", "ssb_kernel_launches", "ssb_destroy")
 
 
@@ -64,11 +66,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_loss_batch.argtypes = [vp, ctypes.POINTER(_Params), i, ctypes.POINTER(ctypes.c_double), vp]
     lib.ssb_reconstruct.argtypes = [vp, ctypes.POINTER(_Params), vp, vp,
                                     ctypes.POINTER(ctypes.c_double), vp]
+    lib.ssb_reconstruct_upsampled.argtypes = [vp, ctypes.POINTER(_Params), i, vp, vp,
+                                              ctypes.POINTER(ctypes.c_double), vp]
     lib.ssb_info.argtypes = [vp, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.ssb_export_g.argtypes = [vp, vp, i, vp]
     lib.ssb_unpack_counts.argtypes = [vp, i, sz, vp, vp]
     lib.ssb_profile_objective.argtypes = [vp, ctypes.POINTER(_Params), ctypes.POINTER(_KernelTime),
                                           i, ctypes.POINTER(i), vp]
+    lib.ssb_profile_reconstruct_upsampled.argtypes = [vp, ctypes.POINTER(_Params), i, vp,
+                                                      ctypes.POINTER(_KernelTime), i,
+                                                      ctypes.POINTER(i), vp]
     lib.ssb_loss_noalloc.argtypes = [ctypes.POINTER(_Geometry), vp, ctypes.POINTER(_Params),
                                      ctypes.POINTER(ctypes.c_double), vp]
     lib.ssb_status_string.argtypes = [i]
@@ -79,8 +86,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_kernel_launches.restype = ctypes.c_uint64
     lib.ssb_destroy.argtypes = [vp]
     lib.ssb_destroy.restype = None
-    for name in ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_info",
-                 "ssb_export_g", "ssb_unpack_counts", "ssb_profile_objective", "ssb_loss_noalloc"):
+    for name in ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_reconstruct_upsampled", "ssb_info",
+                 "ssb_export_g", "ssb_unpack_counts", "ssb_profile_objective",
+                 "ssb_profile_reconstruct_upsampled", "ssb_loss_noalloc"):
         getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -194,6 +202,23 @@ class SSB:
                                          _stream_handle(stream)), "ssb_reconstruct")
         return mp, obj, (float(loss.value) if want_loss else None)
 
+    def reconstruct_upsampled(self, theta, factor: int, want_object: bool = True,
+                              want_loss: bool = True, stream=None):
+        """(phase [fN][fN] float32, object [fN][fN] complex64 or None, loss or None) of the
+        object redrawn band-limited on a scan grid `factor` times finer."""
+        import torch
+        fn = int(factor) * self.N
+        ph = torch.empty((fn, fn), dtype=torch.float32, device="cuda")
+        obj = torch.empty((fn, fn), dtype=torch.complex64, device="cuda") if want_object else None
+        loss = ctypes.c_double(float("nan"))
+        p = _params([theta])
+        _check(self._lib.ssb_reconstruct_upsampled(
+            self._ctx, p, int(factor), ctypes.c_void_p(ph.data_ptr()),
+            ctypes.c_void_p(obj.data_ptr()) if obj is not None else None,
+            ctypes.byref(loss) if want_loss else None, _stream_handle(stream)),
+            "ssb_reconstruct_upsampled")
+        return ph, obj, (float(loss.value) if want_loss else None)
+
     def profile(self, theta, stream=None) -> dict:
         """{kernel name: (launches, total device ms)} for one objective at theta."""
         cap = 64
@@ -202,6 +227,20 @@ class SSB:
         _check(self._lib.ssb_profile_objective(self._ctx, _params([theta]), out, cap,
                                                ctypes.byref(n), _stream_handle(stream)),
                "ssb_profile_objective")
+        return {out[j].name.decode(): (int(out[j].launches), float(out[j].ms))
+                for j in range(min(cap, n.value))}
+
+    def profile_upsampled(self, theta, factor: int, stream=None) -> dict:
+        """{kernel name: (launches, total device ms)} for one upsampled redraw at theta."""
+        import torch
+        cap = 64
+        out = (_KernelTime * cap)()
+        n = ctypes.c_int(0)
+        fn = int(factor) * self.N
+        ph = torch.empty((fn, fn), dtype=torch.float32, device="cuda")
+        _check(self._lib.ssb_profile_reconstruct_upsampled(
+            self._ctx, _params([theta]), int(factor), ctypes.c_void_p(ph.data_ptr()), out, cap,
+            ctypes.byref(n), _stream_handle(stream)), "ssb_profile_reconstruct_upsampled")
         return {out[j].name.decode(): (int(out[j].launches), float(out[j].ms))
                 for j in range(min(cap, n.value))}
 

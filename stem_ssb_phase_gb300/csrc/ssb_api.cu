@@ -111,6 +111,9 @@ struct ssb_ctx {
     int Bk = 0, D = 0;
     int *flag = nullptr;
     size_t g_bytes = 0, scratch_bytes = 0;
+    // upsampled redraw scratch, allocated on first use for the largest factor seen
+    float2 *up_T = nullptr, *up_tab = nullptr;
+    int up_factor = 0;
 
     ObjectiveArgs args() const {
         ObjectiveArgs a;
@@ -144,7 +147,8 @@ struct ssb_ctx {
 static void free_ctx(ssb_ctx *c) {
     if (!c) return;
     void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->S1, c->Osum,
-                    c->loss, c->flag, c->Zring, c->hring, c->rring, c->S2g, c->sync};
+                    c->loss, c->flag, c->Zring, c->hring, c->rring, c->S2g, c->sync,
+                    c->up_T,  c->up_tab};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete c;
@@ -412,18 +416,58 @@ ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phas
     return check_sync(c, s);
 }
 
-ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel_time *out,
-                                 int cap, int *n_out, void *cuda_stream) {
+ssb_status ssb_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int factor,
+                                     float *phase_out, float *object_c64_out, double *loss_out,
+                                     void *cuda_stream) {
     g_last_error.clear();
-    if (!c || !theta || !n_out || (cap > 0 && !out) || cap < 0) return fail(SSB_ERR_ARG, "bad argument");
+    if (!c || !theta || !phase_out) return fail(SSB_ERR_ARG, "NULL argument");
+    if (factor < 1 || factor > SSB_MAX_UPSAMPLE)
+        return fail(SSB_ERR_ARG, "upsampling factor must be in 1.." + std::to_string(SSB_MAX_UPSAMPLE));
     if (!valid_theta(*theta)) return fail(SSB_ERR_ARG, "non-finite theta");
     DeviceGuard dg(c->dev);
     if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
     cudaStream_t s = (cudaStream_t)cuda_stream;
-    Profiler prof;
-    g_prof = &prof;
-    cudaError_t e = evaluate(c, *theta, c->loss, false, s);
-    g_prof = nullptr;
+    if (factor != c->up_factor) {
+        // the interpolation table depends on the factor; T is sized for the largest one
+        SSB_CK(cudaStreamSynchronize(s));
+        if (factor > c->up_factor || !c->up_T) {
+            if (c->up_T) cudaFree(c->up_T);
+            c->up_T = nullptr;
+            if (cudaMalloc((void **)&c->up_T, sizeof(float2) * upsample_scratch_elems(c->N, factor)) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                c->up_factor = 0;
+                return fail(SSB_ERR_OOM, "cannot allocate the upsampling scratch");
+            }
+        }
+        if (c->up_tab) cudaFree(c->up_tab);
+        c->up_tab = nullptr;
+        std::vector<float2> tab;
+        upsample_table(c->N, factor, tab);
+        if (cudaMalloc((void **)&c->up_tab, sizeof(float2) * tab.size()) != cudaSuccess) {
+            cudaGetLastError();
+            c->up_factor = 0;
+            return fail(SSB_ERR_OOM, "cannot allocate the interpolation table");
+        }
+        SSB_CK(cudaMemcpy(c->up_tab, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice));
+        c->up_factor = factor;
+    }
+    const ObjectiveArgs a = c->args();
+    cudaError_t e = evaluate(c, *theta, c->loss, true, s);
+    if (e != cudaSuccess) return cuda_fail(e, "objective launch");
+    if ((e = launch_upsample(a, factor, c->up_tab, c->up_T, phase_out, (float2 *)object_c64_out, s)) !=
+        cudaSuccess)
+        return cuda_fail(e, "upsampling launch");
+    if (loss_out) {
+        SSB_CK(cudaMemcpyAsync(loss_out, c->loss, sizeof(double), cudaMemcpyDeviceToHost, s));
+    }
+    SSB_CK(cudaStreamSynchronize(s));
+    return check_sync(c, s);
+}
+
+// Reads back the events a profiled call recorded: per kernel name, launches and summed ms.
+static ssb_status collect_profile(Profiler &prof, cudaError_t e, cudaStream_t s, ssb_kernel_time *out,
+                                  int cap, int *n_out, const char *what) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     std::vector<ssb_kernel_time> agg;
     for (auto &r : prof.recs) {
@@ -442,10 +486,47 @@ ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel
         agg[j].launches += 1;
         agg[j].ms += ms;
     }
-    if (e != cudaSuccess) return cuda_fail(e, "profiled objective");
+    if (e != cudaSuccess) return cuda_fail(e, what);
     *n_out = (int)agg.size();
     for (int j = 0; j < (int)agg.size() && j < cap; ++j) out[j] = agg[j];
     return SSB_OK;
+}
+
+ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel_time *out,
+                                 int cap, int *n_out, void *cuda_stream) {
+    g_last_error.clear();
+    if (!c || !theta || !n_out || (cap > 0 && !out) || cap < 0) return fail(SSB_ERR_ARG, "bad argument");
+    if (!valid_theta(*theta)) return fail(SSB_ERR_ARG, "non-finite theta");
+    DeviceGuard dg(c->dev);
+    if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    Profiler prof;
+    g_prof = &prof;
+    cudaError_t e = evaluate(c, *theta, c->loss, false, s);
+    g_prof = nullptr;
+    return collect_profile(prof, e, s, out, cap, n_out, "profiled objective");
+}
+
+ssb_status ssb_profile_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int factor,
+                                             float *phase_out, ssb_kernel_time *out, int cap,
+                                             int *n_out, void *cuda_stream) {
+    g_last_error.clear();
+    if (!c || !theta || !phase_out || !n_out || (cap > 0 && !out) || cap < 0)
+        return fail(SSB_ERR_ARG, "bad argument");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    Profiler prof;
+    g_prof = &prof;
+    ssb_status st = ssb_reconstruct_upsampled(c, theta, factor, phase_out, nullptr, nullptr, cuda_stream);
+    g_prof = nullptr;
+    if (st != SSB_OK) {
+        for (auto &r : prof.recs) {
+            cudaEventDestroy(r.a);
+            cudaEventDestroy(r.b);
+        }
+        return st;
+    }
+    DeviceGuard dg(c->dev);
+    return collect_profile(prof, cudaSuccess, s, out, cap, n_out, "profiled upsampled redraw");
 }
 
 ssb_status ssb_info(const ssb_ctx *c, size_t *g_bytes, size_t *scratch_bytes) {

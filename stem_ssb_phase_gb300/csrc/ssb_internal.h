@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "../../include/ssb.h"
 #include "ssb_device.cuh"
 
@@ -80,5 +82,16 @@ cudaError_t run_objective_fused(const ObjectiveArgs &a, const ssb_params &theta,
 // mean phase = S1/n_bf (float32), object = Osum * scale (complex64) if out_obj != nullptr
 cudaError_t launch_finalize(const ObjectiveArgs &a, float *mean_phase, float *out_obj,
                             cudaStream_t s);
+
+// ---- upsampled redraw (ssb_upsample.cu) ----
+// Interpolation table a(d), d = -factor (N - 1) .. factor N - 1 (complex64), and the size
+// of the intermediate T = O A^T (N x factor N complex64).
+size_t upsample_table_elems(int N, int factor);
+size_t upsample_scratch_elems(int N, int factor);
+void upsample_table(int N, int factor, std::vector<float2> &tab);
+// From Osum (filled by an evaluation with want_object): phase [fN][fN] float32 and, if
+// obj_out != nullptr, the object [fN][fN] complex64 on the factor-times finer grid.
+cudaError_t launch_upsample(const ObjectiveArgs &a, int factor, const float2 *tab, float2 *T,
+                            float *phase_out, float2 *obj_out, cudaStream_t s);
 
 }  // namespace ssb
