@@ -153,12 +153,35 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-def source_digest() -> str:
-    """Digest of the library's CUDA/C++ sources, comments and layout excluded."""
-    h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "stem_ssb_phase_gb300", "csrc", "*"))):
+KERNEL_SOURCES = ("stem_ssb_phase_gb300/csrc/ssb_fused.cu", "stem_ssb_phase_gb300/csrc/ssb_device.cuh",
+                  "stem_ssb_phase_gb300/csrc/ssb_regfft.cuh", "stem_ssb_phase_gb300/csrc/ssb_internal.h",
+                  "include/ssb.h")
+
+
+def kernel_includes(path: str) -> list:
+    """In-tree files a source includes with #include "...", followed recursively."""
+    seen, todo = [], [os.path.normpath(path)]
+    while todo:
+        f = todo.pop()
+        if f in seen or not os.path.exists(f):
+            continue
+        seen.append(f)
         with open(f, encoding="utf-8") as fh:
-            h.update(os.path.basename(f).encode())
+            for line in fh:
+                t = line.strip()
+                if t.startswith("#include") and '"' in t:
+                    inc = t.split('"')[1]
+                    todo.append(os.path.normpath(os.path.join(os.path.dirname(f), inc)))
+    return sorted(seen)
+
+
+def source_digest() -> str:
+    """Digest of the sources the fused kernel's translation unit is compiled from
+    (ssb_fused.cu and the in-tree headers it includes), comments and layout excluded."""
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+            h.update(rel.encode())
             h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 

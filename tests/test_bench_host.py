@@ -76,3 +76,10 @@ def test_source_digest_ignores_comments_but_not_code():
     assert bench._code_only(src) == bench._code_only(src.replace("note", "other").replace("\n", "\n\n"))
     assert bench._code_only(src) != bench._code_only(src.replace("a = 1", "a = 2"))
     assert bench._code_only(src) != bench._code_only(src.replace("x // y", "x // z"))
+
+
+def test_source_digest_covers_the_fused_kernels_translation_unit():
+    """The digest lists exactly the files the fused kernel is compiled from."""
+    import bench
+    tu = bench.kernel_includes(os.path.join(ROOT, "stem_ssb_phase_gb300", "csrc", "ssb_fused.cu"))
+    assert sorted(os.path.relpath(f, ROOT) for f in tu) == sorted(bench.KERNEL_SOURCES)
