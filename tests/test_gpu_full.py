@@ -32,11 +32,19 @@ def full_case():
     ctx.close()
 
 
-def test_full_size_loss_and_mean_phase_match_the_oracle(full_case):
+@pytest.fixture(scope="module")
+def full_ref(full_case):
+    """The oracle at the trial the benchmark times, over every BF pixel, with the object."""
+    w, geom, host, _ = full_case
+    theta = ssb_synth.draw_trials(w, 1)[0]
+    return theta, oracle.objective(geom, theta, counts=host, want_object=True,
+                                   workers=min(32, oracle.default_workers()))
+
+
+def test_full_size_loss_and_mean_phase_match_the_oracle(full_case, full_ref):
     w, geom, host, ctx = full_case
-    theta = ssb_synth.draw_trials(w, 1)[0]  # the trial the benchmark times
+    theta, ref = full_ref  # the trial the benchmark times
     mp, _, loss = ctx.reconstruct(theta, want_object=False)
-    ref = oracle.objective(geom, theta, counts=host, workers=min(32, oracle.default_workers()))
     assert abs(loss - ref["loss"]) <= 1e-5 * ref["loss"], (loss, ref["loss"])
     mask = ~ref["branch_cut"]
     err = np.abs(mp.cpu().numpy().astype(np.float64) - ref["mean_phase"])[mask]
@@ -74,3 +82,19 @@ def test_full_size_ssb1_matches_the_oracle(full_case):
     err = np.abs(mp.cpu().numpy().astype(np.float64) - ref["mean_phase"])[mask]
     assert mask.mean() > 0.9
     assert err.max() <= 1e-4, (err.max(), int((err > 1e-4).sum()))
+
+
+def test_full_size_upsampled_redraw_matches_the_oracle(full_case, full_ref):
+    """The 4x redraw the upsampled bench times (2048 x 2048 output) against the oracle's
+    full-size object interpolated by the oracle: object within 1e-5 relative L2, phase
+    within 1e-4 rad (modulo 2 pi) where the modulus is at least 5 % of its RMS."""
+    _, _, _, ctx = full_case
+    theta, ref = full_ref
+    ph, obj, _ = ctx.reconstruct_upsampled(theta, 4)
+    up = oracle.upsample_object(ref["object"], 4)
+    o = obj.cpu().numpy().astype(np.complex128)
+    assert np.linalg.norm(o - up) <= 1e-5 * np.linalg.norm(up)
+    mask = np.abs(up) >= 0.05 * np.sqrt(np.mean(np.abs(up) ** 2))
+    assert mask.mean() > 0.5
+    d = np.angle(np.exp(1j * (ph.cpu().numpy().astype(np.float64) - np.angle(up))))[mask]
+    assert np.abs(d).max() <= 1e-4, np.abs(d).max()
