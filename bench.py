@@ -465,7 +465,11 @@ def run_upsample(args):
     from stem_ssb_phase_gb300 import build as _build
     _build.build()
     w = ssb_synth.WORKLOADS[args.workload]
-    geom, counts, _ = ssb_synth.simulate_counts_torch(w, "cuda")
+    sub = None
+    if args.bf_subset:
+        n_all = ssb_synth.make_geometry(w).n_bf
+        sub = np.linspace(0, n_all - 1, min(args.bf_subset, n_all)).astype(int)
+    geom, counts, _ = ssb_synth.simulate_counts_torch(w, "cuda", geom=ssb_synth.make_geometry(w, bf_subset=sub))
     ctx = ssbgpu.SSB(geom, counts, transfer=args.transfer)
     del counts
     torch.cuda.empty_cache()
