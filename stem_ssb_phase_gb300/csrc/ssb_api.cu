@@ -280,7 +280,7 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     SSB_ALLOC(c->Zring, fused_ring_elems(N, c->Bk, c->D, ssb1), sb);
     SSB_ALLOC(c->hring, fused_hring_elems(N, c->Bk, c->D), sb);
     SSB_ALLOC(c->rring, fused_rring_elems(N, c->Bk, c->D), sb);
-    SSB_ALLOC(c->S2g, (size_t)fused_row_tasks(N), sb);
+    SSB_ALLOC(c->S2g, fused_s2g_elems(N), sb);
     SSB_ALLOC(c->sync, fused_sync_words(N, c->n_bf, c->Bk), sb);
     SSB_ALLOC(c->S1, P, sb);
     SSB_ALLOC(c->Osum, P, sb);

@@ -722,24 +722,45 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
 
 // ---------------------------------------------------------------- loss
 
-__global__ void __launch_bounds__(1024) k_loss_fused(const double *__restrict__ S1,
-                                                     const double *__restrict__ S2g, int nr,
-                                                     int P, double inv_n, double *__restrict__ out) {
-    __shared__ double red[1024];
+// L = (1/P) sum_r [S2(r)/n - (S1(r)/n)^2], with S2 summed per row task.  Each block reduces
+// one contiguous range of pixels in a fixed order (strided per thread, then a shared-memory
+// tree) into part[block]; the block that finishes last (counted in *cnt, cleared with the
+// scheduler words before every evaluation) adds the partials in block order and the row
+// task sums in task order.  The result does not depend on which block finishes last.
+constexpr int kLossBlocks = 128, kLossThreads = 256;
+
+__global__ void __launch_bounds__(kLossThreads) k_loss_fused(const double *__restrict__ S1,
+                                                             const double *__restrict__ S2g, int nr,
+                                                             int P, double inv_n, double *part,
+                                                             unsigned *cnt, double *__restrict__ out) {
+    __shared__ double red[kLossThreads];
+    __shared__ unsigned s_rank;
     const int tid = threadIdx.x;
+    const int per = (P + kLossBlocks - 1) / kLossBlocks;
+    const int i0 = blockIdx.x * per, i1 = min(P, i0 + per);
     double acc = 0.0;
-    for (int i = tid; i < P; i += 1024) {
+    for (int i = i0 + tid; i < i1; i += kLossThreads) {
         const double m = S1[i] * inv_n;
         acc -= m * m;
     }
-    for (int i = tid; i < nr; i += 1024) acc += S2g[i] * inv_n;
     red[tid] = acc;
     __syncthreads();
-    for (int s = 512; s > 0; s >>= 1) {
-        if (tid < s) red[tid] += red[tid + s];
+    for (int h = kLossThreads / 2; h > 0; h >>= 1) {
+        if (tid < h) red[tid] += red[tid + h];
         __syncthreads();
     }
-    if (tid == 0) *out = red[0] / (double)P;
+    if (tid == 0) {
+        part[blockIdx.x] = red[0];
+        __threadfence();
+        s_rank = atomicAdd(cnt, 1u);
+    }
+    __syncthreads();
+    if (s_rank != kLossBlocks - 1 || tid != 0) return;
+    __threadfence();
+    double sm = 0.0, s2 = 0.0;
+    for (int b = 0; b < kLossBlocks; ++b) sm += __ldcg(part + b);
+    for (int r = 0; r < nr; ++r) s2 += S2g[r] * inv_n;
+    *out = (s2 + sm) / (double)P;
 }
 
 // ---------------------------------------------------------------- host side
@@ -749,9 +770,10 @@ static int row_tasks_for(int N) {
     return N / std::min(groups, N);
 }
 
+// scheduler words, then the loss kernel's block counter (the last word)
 size_t fused_sync_words(int N, int n_bf, int Bk) {
     const int nbatch = (n_bf + Bk - 1) / Bk;
-    return 2 + (size_t)nbatch * (1 + 2 * (size_t)Bk) + (size_t)row_tasks_for(N);
+    return 2 + (size_t)nbatch * (1 + 2 * (size_t)Bk) + (size_t)row_tasks_for(N) + 1;
 }
 
 static size_t ldz_for(int N) { return (size_t)((N / 2 + 1 + 7) / 8 * 8); }
@@ -761,6 +783,7 @@ size_t fused_ring_elems(int N, int Bk, int D, bool ssb1) {
 size_t fused_hring_elems(int N, int Bk, int D) { return (size_t)D * Bk * ldz_for(N); }
 size_t fused_rring_elems(int N, int Bk, int D) { return (size_t)D * Bk * (size_t)(N / 2); }
 int fused_row_tasks(int N) { return row_tasks_for(N); }
+size_t fused_s2g_elems(int N) { return (size_t)row_tasks_for(N) + kLossBlocks; }
 
 // cuTensorMapEncodeTiled, resolved once through the runtime (no link against the driver
 // library); null if the driver does not provide it.
@@ -860,7 +883,9 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     e = want_object ? fused_launch<N, true, SSB1>(fp, s) : fused_launch<N, false, SSB1>(fp, s);
     if (e != cudaSuccess) return e;
     prof_begin("k_loss", s);
-    k_loss_fused<<<1, 1024, 0, s>>>(a.S1, a.S2g, S::NR, (int)P, 1.0 / a.n_bf, loss_slot);
+    k_loss_fused<<<kLossBlocks, kLossThreads, 0, s>>>(
+        a.S1, a.S2g, S::NR, (int)P, 1.0 / a.n_bf, a.S2g + S::NR,
+        a.sync + fused_sync_words(N, a.n_bf, a.Bk) - 1, loss_slot);
     prof_end(s);
     count_launch();
     return cudaGetLastError();

@@ -74,6 +74,7 @@ size_t fused_ring_elems(int N, int Bk, int D, bool ssb1 = false);  // ssb1: all 
 size_t fused_hring_elems(int N, int Bk, int D);
 size_t fused_rring_elems(int N, int Bk, int D);
 int fused_row_tasks(int N);
+size_t fused_s2g_elems(int N);  // per row task S2 sums, then the loss kernel's block partials
 // One full objective evaluation on the persistent fused kernel (accumulators and
 // scheduler words cleared first), loss written to *loss_slot.
 cudaError_t run_objective_fused(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,

@@ -63,7 +63,7 @@ static NoallocLayout noalloc_layout(int N, int n_bf) {
     L.Z = o;      o = up256(o + fused_ring_elems(N, bk, kNoallocRing) * sizeof(float2));
     L.h = o;      o = up256(o + fused_hring_elems(N, bk, kNoallocRing) * sizeof(float2));
     L.rp = o;     o = up256(o + fused_rring_elems(N, bk, kNoallocRing) * sizeof(float2));
-    L.S2g = o;    o = up256(o + (size_t)fused_row_tasks(N) * sizeof(double));
+    L.S2g = o;    o = up256(o + fused_s2g_elems(N) * sizeof(double));
     L.kgeo = o;   o = up256(o + (size_t)n_bf * sizeof(float4));
     L.kalpha = o; o = up256(o + (size_t)n_bf * sizeof(double2));
     L.kturn = o;  o = up256(o + (size_t)n_bf * sizeof(uint2));
