@@ -453,12 +453,23 @@ def upsample_flops(n: int, factor: int) -> float:
     return 8.0 * (n * n * fn + fn * fn * n)
 
 
+def redraw_algorithmic_bytes(n_bf: int, n: int) -> int:
+    """G bytes the spectral sum reads once: n_bf half-plane caches of complex64."""
+    return n_bf * (n // 2 + 1) * n * 8
+
+
 def run_upsample(args):
-    """Upsampled object redraw at the benchmark trial: one objective with the object
-    accumulated, then the band-limited interpolation onto the factor-times finer grid.
-    Reports the whole call per redraw (device events around the C-ABI call, output
-    resident on the device) and, from the per-launch profiler, the two interpolation
-    kernels against the FP32 issue peak of the CUDA cores."""
+    """Object redraw at the benchmark trial, on the device, through the C ABI.
+
+    --upsample F: ssb_reconstruct_upsampled, the objective (with the native loss) and the
+    object sum in one pass, then the band-limited interpolation (roofline of the two
+    k_upsample launches against the FP32 FMA issue peak).
+    --redraw F: ssb_redraw, the phase-of-mean without the loss, from the spectral sum
+    over the BF pixels and one 2-D inverse transform (roofline of k_redraw_sum, which
+    reads the G cache once, against the measured HBM bandwidth), then the interpolation
+    when F > 1.
+    value = ms per redraw from CUDA events around the calls; the per-kernel split from a
+    profiling session over the same number of further calls."""
     import torch
 
     import stem_ssb_phase_gb300 as ssbgpu
@@ -473,11 +484,18 @@ def run_upsample(args):
     ctx = ssbgpu.SSB(geom, counts, transfer=args.transfer)
     del counts
     torch.cuda.empty_cache()
-    f = args.upsample
+    phase_only = bool(args.redraw)
+    f = args.redraw if phase_only else args.upsample
     n = geom.scan_n
     theta = ssb_synth.draw_trials(w, 1)[0]
+
+    def call():
+        if phase_only:
+            return ctx.redraw(theta, f)
+        return ctx.reconstruct_upsampled(theta, f)
+
     for _ in range(args.warmup):
-        ctx.reconstruct_upsampled(theta, f)
+        call()
     stream = torch.cuda.current_stream()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
@@ -486,35 +504,48 @@ def run_upsample(args):
     torch.cuda.synchronize()
     ev[0].record(stream)
     for _ in range(args.steps):
-        ph, obj, loss = ctx.reconstruct_upsampled(theta, f)
+        out = call()
     ev[1].record(stream)
     torch.cuda.synchronize()
     launches = ssbgpu.kernel_launches() - l0
     ms = ev[0].elapsed_time(ev[1]) / args.steps
-    prof = {}
-    for _ in range(args.steps):
-        for k, (c, t) in ctx.profile_upsampled(theta, f).items():
-            a = prof.setdefault(k, [0, 0.0])
-            a[0] += c
-            a[1] += t
+    ssbgpu.profile_begin()
+    try:
+        for _ in range(args.steps):
+            call()
+    finally:
+        prof = ssbgpu.profile_end()
     clk = clocks.stop()
-    up_ms = sum(t for k, (c, t) in prof.items() if k.startswith("k_upsample")) / args.steps
+    per = {k: t / args.steps for k, (c, t) in sorted(prof.items())}
+    up_ms = sum(t for k, t in per.items() if k.startswith("k_upsample"))
     sm_mhz = clk["sm_mhz"] if clk else 2070.0
-    peak = fp32_alu_peak_tflops(sm_mhz)
-    achieved = upsample_flops(n, f) / (up_ms * 1e-3) / 1e12
-    out = {"metric": "upsampled object redraw (objective + band-limited interpolation), ms per redraw",
-           "value": ms, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+    hbm, kind = _peaks()
+    if phase_only:
+        sum_ms = per.get("k_redraw_sum", float("nan"))
+        gbytes = redraw_algorithmic_bytes(geom.n_bf, n) / 1e9
+        achieved = gbytes / (sum_ms * 1e-3)
+        roof = {"bound": "hbm", "kernel": "k_redraw_sum", "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                "algorithmic_bytes_per_launch": redraw_algorithmic_bytes(geom.n_bf, n),
+                "peak_kind": "%s hbm_gbs (copy)" % kind}
+        metric = "phase-of-mean redraw without the loss (spectral sum + one 2-D inverse transform), ms per redraw"
+    else:
+        peak = fp32_alu_peak_tflops(sm_mhz)
+        achieved = upsample_flops(n, f) / (up_ms * 1e-3) / 1e12 if up_ms > 0 else None
+        roof = {"bound": "alu", "kernel": "k_upsample", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak if achieved else None, "traffic": None,
+                "peak_basis": "FP32 FMA issue, 152 SMs x 128 lanes x 2 at the median SM clock"}
+        metric = "upsampled object redraw (objective + band-limited interpolation), ms per redraw"
+    res = {"metric": metric, "value": ms, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
            "steps": args.steps, "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
            "config": {"workload": "%s: %dx%d scan, %d BF" % (w.name, n, n, geom.n_bf),
                       "upsample": f, "output": "%dx%d phase + complex64 object" % (f * n, f * n),
-                      "transfer": args.transfer},
-           "kernels_ms_per_redraw": {k: t / args.steps for k, (c, t) in sorted(prof.items())},
-           "upsample_ms": up_ms,
-           "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak, "traffic": None,
-                        "peak_basis": "FP32 FMA issue, 152 SMs x 128 lanes x 2 at the median SM clock"},
-           "gpu_launches": launches, "clocks": clk, "loss": loss}
-    print(json.dumps(out), flush=True)
+                      "loss": not phase_only, "transfer": args.transfer},
+           "kernels_ms_per_redraw": per, "upsample_ms": up_ms, "roofline": roof,
+           "gpu_launches": launches, "clocks": clk}
+    if not phase_only:
+        res["loss"] = out[2]
+    print(json.dumps(res), flush=True)
     ctx.close()
 
 
@@ -570,7 +601,9 @@ def main():
     ap.add_argument("--fit", action="store_true",
                     help="time the full fit workload (200 trials + Nelder-Mead + redraw) instead")
     ap.add_argument("--upsample", type=int, default=0,
-                    help="time the upsampled object redraw at this factor (1-8) instead")
+                    help="time the upsampled object redraw with the loss at this factor (1-8) instead")
+    ap.add_argument("--redraw", type=int, default=0,
+                    help="time the phase-of-mean redraw without the loss at this factor (1-8) instead")
     ap.add_argument("--bf-subset", type=int, default=0,
                     help="evenly spaced BF pixels of the workload (profiling a small case)")
     args = ap.parse_args()
@@ -590,7 +623,7 @@ def main():
         if args.fit:
             if rank == 0:
                 run_fit(args)
-        elif args.upsample and args.impl == "ours":
+        elif (args.upsample or args.redraw) and args.impl == "ours":
             if rank == 0:
                 run_upsample(args)
         elif args.impl == "reference":

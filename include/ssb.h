@@ -128,6 +128,22 @@ ssb_status ssb_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int fa
                                      float *phase_out, float *object_c64_out, double *loss_out,
                                      void *cuda_stream);
 
+/* Phase-of-mean redraw without the loss (page "Later SSB performance checkpoints", joint
+ * calibration section: output reconstruction "phase only", factors 1 to 4).  The object
+ * O = (1/n_bf) sum_k c_k is computed through its spectrum, O = (1/n_bf) IFFT2[sum_k C_k]
+ * (equal by linearity): one sum of the corrected spectra over the BF pixels and a single
+ * 2-D inverse transform, with no per-BF transform, phase or moment.  The correction and the
+ * transfer are the objective's; the BF sum runs in 32 fixed slices (float32 within runs of
+ * 32 BF pixels, float64 across), so results are run-to-run identical.  factor > 1 then
+ * interpolates as ssb_reconstruct_upsampled does.
+ *   factor:         1 .. SSB_MAX_UPSAMPLE
+ *   phase_out:      device [factor N][factor N] float32, arg O              (required)
+ *   object_c64_out: device [factor N][factor N] complex64 interleaved, O     (nullable)
+ * The context allocates the slice sums (32 N^2 complex128) and two N^2 complex64 buffers
+ * on the first call (not counted by ssb_info); SSB_ERR_OOM if that fails. */
+ssb_status ssb_redraw(ssb_ctx *c, const ssb_params *theta, int factor, float *phase_out,
+                      float *object_c64_out, void *cuda_stream);
+
 /* Sizes of the G cache and of the scratch the context holds (either pointer nullable). */
 ssb_status ssb_info(const ssb_ctx *c, size_t *g_bytes, size_t *scratch_bytes);
 
@@ -154,12 +170,15 @@ typedef struct {
 ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel_time *out,
                                  int cap, int *n_out, void *cuda_stream);
 
-/* The same per-kernel timing for one ssb_reconstruct_upsampled call (objective, then the
- * two interpolation products): phase_out as there (device [factor N][factor N] float32);
- * errors as there.  Synchronises the stream. */
-ssb_status ssb_profile_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int factor,
-                                             float *phase_out, ssb_kernel_time *out, int cap,
-                                             int *n_out, void *cuda_stream);
+/* Per-kernel timing of every library call this thread makes between ssb_profile_begin
+ * and ssb_profile_end (tracing aid): each launch gets a CUDA event pair on the stream it
+ * runs on.  ssb_profile_end waits for those events and reports, per kernel name, the
+ * launch count and the summed device time in milliseconds, as ssb_profile_objective does
+ * (out: host [cap]; *n_out: distinct kernels).  One session per thread at a time;
+ * ssb_profile_begin with a session (or ssb_profile_objective) already open on the thread,
+ * or ssb_profile_end without one, gives SSB_ERR_ARG. */
+ssb_status ssb_profile_begin(void);
+ssb_status ssb_profile_end(ssb_kernel_time *out, int cap, int *n_out);
 
 /* Loss of one trial without any device allocation.  (The pages have no counterpart: this
  * entry point exists for callers of this library that cannot allocate device memory when

@@ -23,8 +23,8 @@ STATUS = {0: "SSB_OK", 1: "SSB_ERR_ARG", 2: "SSB_ERR_UNSUPPORTED", 3: "SSB_ERR_O
 # every symbol include/ssb.h declares
 EXPORTS = ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_reconstruct_upsampled",
            "ssb_info", "ssb_export_g",
-           "ssb_unpack_counts", "ssb_profile_objective", "ssb_profile_reconstruct_upsampled",
-           "ssb_loss_noalloc", "ssb_status_string",
+           "ssb_unpack_counts", "ssb_profile_objective", "ssb_profile_begin", "ssb_profile_end",
+           "ssb_redraw", "ssb_loss_noalloc", "ssb_status_string",
            "ssb_last_error", "ssb_kernel_launches", "ssb_destroy")
 
 
@@ -73,9 +73,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_unpack_counts.argtypes = [vp, i, sz, vp, vp]
     lib.ssb_profile_objective.argtypes = [vp, ctypes.POINTER(_Params), ctypes.POINTER(_KernelTime),
                                           i, ctypes.POINTER(i), vp]
-    lib.ssb_profile_reconstruct_upsampled.argtypes = [vp, ctypes.POINTER(_Params), i, vp,
-                                                      ctypes.POINTER(_KernelTime), i,
-                                                      ctypes.POINTER(i), vp]
+    lib.ssb_profile_begin.argtypes = []
+    lib.ssb_profile_end.argtypes = [ctypes.POINTER(_KernelTime), i, ctypes.POINTER(i)]
+    lib.ssb_redraw.argtypes = [vp, ctypes.POINTER(_Params), i, vp, vp, vp]
     lib.ssb_loss_noalloc.argtypes = [ctypes.POINTER(_Geometry), vp, ctypes.POINTER(_Params),
                                      ctypes.POINTER(ctypes.c_double), vp]
     lib.ssb_status_string.argtypes = [i]
@@ -88,7 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_destroy.restype = None
     for name in ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_reconstruct_upsampled", "ssb_info",
                  "ssb_export_g", "ssb_unpack_counts", "ssb_profile_objective",
-                 "ssb_profile_reconstruct_upsampled", "ssb_loss_noalloc"):
+                 "ssb_profile_begin", "ssb_profile_end", "ssb_redraw", "ssb_loss_noalloc"):
         getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -230,19 +230,18 @@ class SSB:
         return {out[j].name.decode(): (int(out[j].launches), float(out[j].ms))
                 for j in range(min(cap, n.value))}
 
-    def profile_upsampled(self, theta, factor: int, stream=None) -> dict:
-        """{kernel name: (launches, total device ms)} for one upsampled redraw at theta."""
+    def redraw(self, theta, factor: int = 1, want_object: bool = True, stream=None):
+        """(phase arg O [fN][fN] float32, object O [fN][fN] complex64 or None): the
+        phase-of-mean redraw from the spectral sum, without the loss."""
         import torch
-        cap = 64
-        out = (_KernelTime * cap)()
-        n = ctypes.c_int(0)
         fn = int(factor) * self.N
         ph = torch.empty((fn, fn), dtype=torch.float32, device="cuda")
-        _check(self._lib.ssb_profile_reconstruct_upsampled(
-            self._ctx, _params([theta]), int(factor), ctypes.c_void_p(ph.data_ptr()), out, cap,
-            ctypes.byref(n), _stream_handle(stream)), "ssb_profile_reconstruct_upsampled")
-        return {out[j].name.decode(): (int(out[j].launches), float(out[j].ms))
-                for j in range(min(cap, n.value))}
+        obj = torch.empty((fn, fn), dtype=torch.complex64, device="cuda") if want_object else None
+        p = _params([theta])
+        _check(self._lib.ssb_redraw(self._ctx, p, int(factor), ctypes.c_void_p(ph.data_ptr()),
+                                    ctypes.c_void_p(obj.data_ptr()) if obj is not None else None,
+                                    _stream_handle(stream)), "ssb_redraw")
+        return ph, obj
 
     def export_g(self, stream=None):
         """The G cache as a CUDA complex64 tensor [n_bf][N/2+1][N] (Qx-major, Qy contiguous)."""
@@ -262,6 +261,22 @@ class SSB:
             self.close()
         except Exception:
             pass
+
+
+def profile_begin():
+    """Start timing every library launch this thread makes (see profile_end)."""
+    _check(load_library().ssb_profile_begin(), "ssb_profile_begin")
+
+
+def profile_end() -> dict:
+    """{kernel name: (launches, total device ms)} since profile_begin on this thread."""
+    lib = load_library()
+    cap = 64
+    out = (_KernelTime * cap)()
+    n = ctypes.c_int(0)
+    _check(lib.ssb_profile_end(out, cap, ctypes.byref(n)), "ssb_profile_end")
+    return {out[j].name.decode(): (int(out[j].launches), float(out[j].ms))
+            for j in range(min(cap, n.value))}
 
 
 def unpack_counts(counts, stream=None):

@@ -114,6 +114,9 @@ struct ssb_ctx {
     // upsampled redraw scratch, allocated on first use for the largest factor seen
     float2 *up_T = nullptr, *up_tab = nullptr;
     int up_factor = 0;
+    // redraw-without-loss scratch, allocated on first use
+    double2 *rd_part = nullptr;
+    float2 *rd_S = nullptr, *rd_T = nullptr;
 
     ObjectiveArgs args() const {
         ObjectiveArgs a;
@@ -148,7 +151,7 @@ static void free_ctx(ssb_ctx *c) {
     if (!c) return;
     void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->S1, c->Osum,
                     c->loss, c->flag, c->Zring, c->hring, c->rring, c->S2g, c->sync,
-                    c->up_T,  c->up_tab};
+                    c->up_T,  c->up_tab, c->rd_part, c->rd_S, c->rd_T};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete c;
@@ -416,6 +419,52 @@ ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phas
     return check_sync(c, s);
 }
 
+// Interpolation table and intermediate for `factor` (regrown for a larger factor).
+static ssb_status ensure_upsample(ssb_ctx *c, int factor, cudaStream_t s) {
+    if (factor == c->up_factor && c->up_T && c->up_tab) return SSB_OK;
+    SSB_CK(cudaStreamSynchronize(s));
+    if (factor > c->up_factor || !c->up_T) {
+        if (c->up_T) cudaFree(c->up_T);
+        c->up_T = nullptr;
+        if (cudaMalloc((void **)&c->up_T, sizeof(float2) * upsample_scratch_elems(c->N, factor)) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            c->up_factor = 0;
+            return fail(SSB_ERR_OOM, "cannot allocate the upsampling scratch");
+        }
+    }
+    if (c->up_tab) cudaFree(c->up_tab);
+    c->up_tab = nullptr;
+    std::vector<float2> tab;
+    upsample_table(c->N, factor, tab);
+    if (cudaMalloc((void **)&c->up_tab, sizeof(float2) * tab.size()) != cudaSuccess) {
+        cudaGetLastError();
+        c->up_factor = 0;
+        return fail(SSB_ERR_OOM, "cannot allocate the interpolation table");
+    }
+    SSB_CK(cudaMemcpy(c->up_tab, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice));
+    c->up_factor = factor;
+    return SSB_OK;
+}
+
+// Slice sums, spectral sum and transform buffers of the redraw without the loss.
+static ssb_status ensure_redraw(ssb_ctx *c) {
+    if (c->rd_part && c->rd_S && c->rd_T) return SSB_OK;
+    const size_t P = (size_t)c->N * c->N;
+    if (cudaMalloc((void **)&c->rd_part, sizeof(double2) * redraw_part_elems(c->N, c->n_bf)) != cudaSuccess ||
+        cudaMalloc((void **)&c->rd_S, sizeof(float2) * P) != cudaSuccess ||
+        cudaMalloc((void **)&c->rd_T, sizeof(float2) * P) != cudaSuccess) {
+        cudaGetLastError();
+        void *ptrs[] = {c->rd_part, c->rd_S, c->rd_T};
+        for (void *q : ptrs)
+            if (q) cudaFree(q);
+        c->rd_part = nullptr;
+        c->rd_S = c->rd_T = nullptr;
+        return fail(SSB_ERR_OOM, "cannot allocate the redraw scratch");
+    }
+    return SSB_OK;
+}
+
 ssb_status ssb_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int factor,
                                      float *phase_out, float *object_c64_out, double *loss_out,
                                      void *cuda_stream) {
@@ -427,31 +476,8 @@ ssb_status ssb_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int fa
     DeviceGuard dg(c->dev);
     if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
     cudaStream_t s = (cudaStream_t)cuda_stream;
-    if (factor != c->up_factor) {
-        // the interpolation table depends on the factor; T is sized for the largest one
-        SSB_CK(cudaStreamSynchronize(s));
-        if (factor > c->up_factor || !c->up_T) {
-            if (c->up_T) cudaFree(c->up_T);
-            c->up_T = nullptr;
-            if (cudaMalloc((void **)&c->up_T, sizeof(float2) * upsample_scratch_elems(c->N, factor)) !=
-                cudaSuccess) {
-                cudaGetLastError();
-                c->up_factor = 0;
-                return fail(SSB_ERR_OOM, "cannot allocate the upsampling scratch");
-            }
-        }
-        if (c->up_tab) cudaFree(c->up_tab);
-        c->up_tab = nullptr;
-        std::vector<float2> tab;
-        upsample_table(c->N, factor, tab);
-        if (cudaMalloc((void **)&c->up_tab, sizeof(float2) * tab.size()) != cudaSuccess) {
-            cudaGetLastError();
-            c->up_factor = 0;
-            return fail(SSB_ERR_OOM, "cannot allocate the interpolation table");
-        }
-        SSB_CK(cudaMemcpy(c->up_tab, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice));
-        c->up_factor = factor;
-    }
+    ssb_status st = ensure_upsample(c, factor, s);
+    if (st != SSB_OK) return st;
     const ObjectiveArgs a = c->args();
     cudaError_t e = evaluate(c, *theta, c->loss, true, s);
     if (e != cudaSuccess) return cuda_fail(e, "objective launch");
@@ -465,13 +491,39 @@ ssb_status ssb_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int fa
     return check_sync(c, s);
 }
 
+ssb_status ssb_redraw(ssb_ctx *c, const ssb_params *theta, int factor, float *phase_out,
+                      float *object_c64_out, void *cuda_stream) {
+    g_last_error.clear();
+    if (!c || !theta || !phase_out) return fail(SSB_ERR_ARG, "NULL argument");
+    if (factor < 1 || factor > SSB_MAX_UPSAMPLE)
+        return fail(SSB_ERR_ARG, "upsampling factor must be in 1.." + std::to_string(SSB_MAX_UPSAMPLE));
+    if (!valid_theta(*theta)) return fail(SSB_ERR_ARG, "non-finite theta");
+    DeviceGuard dg(c->dev);
+    if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    ssb_status st = ensure_redraw(c);
+    if (st != SSB_OK) return st;
+    if (factor > 1 && (st = ensure_upsample(c, factor, s)) != SSB_OK) return st;
+    const ObjectiveArgs a = c->args();
+    cudaError_t e = launch_redraw(a, *theta, c->rd_part, c->rd_S, c->rd_T,
+                                  factor == 1 ? phase_out : nullptr,
+                                  factor == 1 ? (float2 *)object_c64_out : nullptr, s);
+    if (e != cudaSuccess) return cuda_fail(e, "redraw launch");
+    if (factor > 1 &&
+        (e = launch_upsample(a, factor, c->up_tab, c->up_T, phase_out, (float2 *)object_c64_out, s)) !=
+            cudaSuccess)
+        return cuda_fail(e, "upsampling launch");
+    SSB_CK(cudaStreamSynchronize(s));
+    return SSB_OK;
+}
+
 // Reads back the events a profiled call recorded: per kernel name, launches and summed ms.
-static ssb_status collect_profile(Profiler &prof, cudaError_t e, cudaStream_t s, ssb_kernel_time *out,
-                                  int cap, int *n_out, const char *what) {
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+static ssb_status collect_profile(Profiler &prof, cudaError_t e, ssb_kernel_time *out, int cap,
+                                  int *n_out, const char *what) {
     std::vector<ssb_kernel_time> agg;
     for (auto &r : prof.recs) {
         float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventSynchronize(r.b);
         if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
         cudaEventDestroy(r.a);
         cudaEventDestroy(r.b);
@@ -500,33 +552,44 @@ ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel
     DeviceGuard dg(c->dev);
     if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
     cudaStream_t s = (cudaStream_t)cuda_stream;
+    if (g_prof) return fail(SSB_ERR_ARG, "a profiling session is open on this thread");
     Profiler prof;
     g_prof = &prof;
     cudaError_t e = evaluate(c, *theta, c->loss, false, s);
     g_prof = nullptr;
-    return collect_profile(prof, e, s, out, cap, n_out, "profiled objective");
+    return collect_profile(prof, e, out, cap, n_out, "profiled objective");
 }
 
-ssb_status ssb_profile_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int factor,
-                                             float *phase_out, ssb_kernel_time *out, int cap,
-                                             int *n_out, void *cuda_stream) {
+static thread_local Profiler *g_session = nullptr;
+
+ssb_status ssb_profile_begin(void) {
     g_last_error.clear();
-    if (!c || !theta || !phase_out || !n_out || (cap > 0 && !out) || cap < 0)
-        return fail(SSB_ERR_ARG, "bad argument");
-    cudaStream_t s = (cudaStream_t)cuda_stream;
-    Profiler prof;
-    g_prof = &prof;
-    ssb_status st = ssb_reconstruct_upsampled(c, theta, factor, phase_out, nullptr, nullptr, cuda_stream);
+    if (g_prof) return fail(SSB_ERR_ARG, "a profiling session is already open on this thread");
+    g_session = new (std::nothrow) Profiler;
+    if (!g_session) return fail(SSB_ERR_OOM, "cannot allocate the profiler");
+    g_prof = g_session;
+    return SSB_OK;
+}
+
+ssb_status ssb_profile_end(ssb_kernel_time *out, int cap, int *n_out) {
+    g_last_error.clear();
+    if (!g_session || g_prof != g_session) return fail(SSB_ERR_ARG, "no profiling session is open on this thread");
     g_prof = nullptr;
-    if (st != SSB_OK) {
-        for (auto &r : prof.recs) {
+    Profiler *prof = g_session;
+    g_session = nullptr;
+    ssb_status st;
+    if (!n_out || cap < 0 || (cap > 0 && !out)) {
+        for (auto &r : prof->recs) {
+            cudaEventSynchronize(r.b);
             cudaEventDestroy(r.a);
             cudaEventDestroy(r.b);
         }
-        return st;
+        st = fail(SSB_ERR_ARG, "bad argument");
+    } else {
+        st = collect_profile(*prof, cudaSuccess, out, cap, n_out, "profiling session");
     }
-    DeviceGuard dg(c->dev);
-    return collect_profile(prof, cudaSuccess, s, out, cap, n_out, "profiled upsampled redraw");
+    delete prof;
+    return st;
 }
 
 ssb_status ssb_info(const ssb_ctx *c, size_t *g_bytes, size_t *scratch_bytes) {

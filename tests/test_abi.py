@@ -47,6 +47,8 @@ def test_null_arguments_fail_before_any_device_work(lib):
     assert lib.ssb_loss_batch(None, None, 1, None, None) == 1
     assert lib.ssb_reconstruct(None, None, None, None, None, None) == 1
     assert lib.ssb_reconstruct_upsampled(None, None, 2, None, None, None, None) == 1
+    assert lib.ssb_redraw(None, None, 1, None, None, None) == 1
+    assert lib.ssb_profile_end(None, 0, None) == 1  # no session open
     assert lib.ssb_info(None, None, None) == 1
     assert lib.ssb_export_g(None, None, 0, None) == 1
 
