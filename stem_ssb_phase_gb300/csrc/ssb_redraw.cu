@@ -28,7 +28,7 @@ namespace ssb {
 namespace {
 
 constexpr int kRdThreads = 128;  // threads per block of the spectral sum
-constexpr int kRdBins = 4;       // bins per thread, rows ny = jj + (N / 4) r
+constexpr int kRdBins = 4;       // bins per thread, rows ny = jj + (N / kRdBins) r
 constexpr int kRdRun = 32;       // BF planes summed in float32 before the float64 update
 constexpr int kRdSlices = 32;    // BF slices of the spectral sum (fixed: the result is
                                  // the same on every device)
@@ -63,25 +63,51 @@ __device__ __forceinline__ void flush(double2 &t, float2 &a) {
     a = make_float2(0.f, 0.f);
 }
 
-// Block (x: column group, y: BF slice).  Thread jj of a column holds rows jj + (N/4) r.
+// The column's G values of plane k (none when the column carries no transfer there).
+template <int N, bool SSB1>
+__device__ __forceinline__ void rd_load(const float2 *__restrict__ G, int k, int nx, int jj, bool zero,
+                                        float2 (&gv)[kRdBins]) {
+    constexpr int TPC = N / kRdBins, HG = N / 2 + 1;
+    if (zero) return;
+    if (!SSB1 || nx <= N / 2) {
+        const float2 *g = G + ((size_t)k * HG + nx) * N + jj;
+#pragma unroll
+        for (int r = 0; r < kRdBins; ++r) gv[r] = __ldcs(g + TPC * r);
+    } else {  // G(nx, ny) = conj G(N - nx, N - ny), row index mod N
+        const float2 *g = G + ((size_t)k * HG + (N - nx)) * N;
+#pragma unroll
+        for (int r = 0; r < kRdBins; ++r) gv[r] = cconj(__ldcs(g + ((N - jj - TPC * r) & (N - 1))));
+    }
+}
+
+// Block (x: column group, y: BF slice).  Thread jj of a column holds rows jj + TPC r.  The
+// slice's per-BF geometry is staged in shared memory, and the G values of the next plane
+// are loaded while the current plane is corrected.
 template <int N, bool SSB1>
 __global__ void __launch_bounds__(kRdThreads) k_redraw_sum(RedrawArgs p) {
     constexpr int TPC = N / kRdBins;                      // threads per column
     constexpr int CPB = TPC >= kRdThreads ? 1 : kRdThreads / TPC;  // columns per block
     constexpr int NCOL = SSB1 ? N : N / 2 + 1;
-    constexpr int HG = N / 2 + 1;
     static_assert(TPC <= kRdThreads && kRdThreads % TPC == 0, "column split");
+    extern __shared__ float4 rd_geo[];                    // [kps], then uint2 [kps]
+    uint2 *rd_bt = (uint2 *)(rd_geo + p.kps);
+    const int k0 = blockIdx.y * p.kps, k1 = min(p.n_bf, k0 + p.kps);
+    const int nk = max(0, k1 - k0);
+    for (int i = threadIdx.x; i < nk; i += kRdThreads) {
+        rd_geo[i] = __ldg(p.kgeo + k0 + i);
+        rd_bt[i] = __ldg(p.kturn + k0 + i);
+    }
+    __syncthreads();
     const int jj = threadIdx.x % TPC;
     const int nx = blockIdx.x * CPB + threadIdx.x / TPC;
     if (nx >= NCOL) return;  // no block-level synchronisation below
     const int sx = nx < N / 2 ? nx : nx - N;
-    const int k0 = blockIdx.y * p.kps, k1 = min(p.n_bf, k0 + p.kps);
     const TrialConst &tc = p.tc;
     float2 e[kRdBins];
 #pragma unroll
     for (int r = 0; r < kRdBins; ++r) e[r] = __ldg(p.E + (size_t)nx * N + jj + TPC * r);
-    // SSB2: the thread holding row N/2 (jj = 0, r = 2) of a column 1..N/2-1 also sums the
-    // mirror Nyquist bin (N - nx, N/2)
+    // SSB2: the thread holding row N/2 (jj = 0, r = kRdBins / 2) of a column 1..N/2-1 also
+    // sums the mirror Nyquist bin (N - nx, N/2)
     const bool nyq = !SSB1 && jj == 0 && nx >= 1 && nx < N / 2;
     const float2 em = nyq ? __ldg(p.E + (size_t)(N - nx) * N + N / 2) : make_float2(0.f, 0.f);
     double2 tot[kRdBins];
@@ -93,23 +119,20 @@ __global__ void __launch_bounds__(kRdThreads) k_redraw_sum(RedrawArgs p) {
     }
     double2 totm = make_double2(0.0, 0.0);
     float2 accm = make_float2(0.f, 0.f);
-    for (int k = k0; k < k1; ++k) {
-        const float4 geo = __ldg(p.kgeo + k);
-        const uint2 bt = __ldg(p.kturn + k);
-        const bool active = geo.z > 0.0f;
-        const bool zero = nx > 0 && (!active || (SSB1 ? column_zero1(sx, geo.x, geo.y, tc)
-                                                       : column_zero(sx, geo.x, geo.y, tc)));
+    auto is_zero = [&](float4 geo) {
+        return nx > 0 && (!(geo.z > 0.0f) || (SSB1 ? column_zero1(sx, geo.x, geo.y, tc)
+                                                   : column_zero(sx, geo.x, geo.y, tc)));
+    };
+    float2 gv[kRdBins], gn[kRdBins];
+    bool zero = nk > 0 ? is_zero(rd_geo[0]) : true;
+    rd_load<N, SSB1>(p.G, k0, nx, jj, zero, gv);
+    for (int it = 0; it < nk; ++it) {
+        const float4 geo = rd_geo[it];
+        const uint2 bt = rd_bt[it];
+        const bool zn = it + 1 < nk ? is_zero(rd_geo[it + 1]) : true;
+        rd_load<N, SSB1>(p.G, k0 + it + 1, nx, jj, zn, gn);
         if (!zero) {
-            float2 gv[kRdBins];
-            if (!SSB1 || nx <= N / 2) {
-                const float2 *g = p.G + ((size_t)k * HG + nx) * N + jj;
-#pragma unroll
-                for (int r = 0; r < kRdBins; ++r) gv[r] = __ldcs(g + TPC * r);
-            } else {  // G(nx, ny) = conj G(N - nx, N - ny), row index mod N
-                const float2 *g = p.G + ((size_t)k * HG + (N - nx)) * N;
-#pragma unroll
-                for (int r = 0; r < kRdBins; ++r) gv[r] = cconj(__ldcs(g + ((N - jj - TPC * r) & (N - 1))));
-            }
+            const bool active = geo.z > 0.0f;
             const ColGeom cg = col_geom(sx, geo.x, geo.y, tc);
             const uint32_t phx = bt.x * (uint32_t)sx;
 #pragma unroll
@@ -128,15 +151,18 @@ __global__ void __launch_bounds__(kRdThreads) k_redraw_sum(RedrawArgs p) {
                 // column geometry has p0 negated and the x part of B is negated
                 ColGeom cm = cg;
                 cm.p0 = -cg.p0;
-                cadd_to(accm, correct_ssb2(cconj(gv[2]), -(float)(N / 2), -N / 2, em, cm, 0u - phx,
-                                           bt.y, tc));
+                cadd_to(accm, correct_ssb2(cconj(gv[kRdBins / 2]), -(float)(N / 2), -N / 2, em, cm,
+                                           0u - phx, bt.y, tc));
             }
         }
-        if (((k - k0) % kRdRun) == kRdRun - 1) {
+        if ((it % kRdRun) == kRdRun - 1) {
 #pragma unroll
             for (int r = 0; r < kRdBins; ++r) flush(tot[r], acc[r]);
             flush(totm, accm);
         }
+        zero = zn;
+#pragma unroll
+        for (int r = 0; r < kRdBins; ++r) gv[r] = gn[r];
     }
 #pragma unroll
     for (int r = 0; r < kRdBins; ++r) flush(tot[r], acc[r]);
@@ -213,8 +239,14 @@ cudaError_t redraw_n(RedrawArgs &r, cudaStream_t s) {
     constexpr int TPC = N / kRdBins;
     constexpr int CPB = TPC >= kRdThreads ? 1 : kRdThreads / TPC;
     constexpr int NCOL = SSB1 ? N : N / 2 + 1;
+    const size_t smem = (sizeof(float4) + sizeof(uint2)) * (size_t)r.kps;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_redraw_sum<N, SSB1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
     prof_begin("k_redraw_sum", s);
-    k_redraw_sum<N, SSB1><<<dim3((NCOL + CPB - 1) / CPB, r.slices), kRdThreads, 0, s>>>(r);
+    k_redraw_sum<N, SSB1><<<dim3((NCOL + CPB - 1) / CPB, r.slices), kRdThreads, smem, s>>>(r);
     prof_end(s);
     count_launch();
     prof_begin("k_redraw_combine", s);
