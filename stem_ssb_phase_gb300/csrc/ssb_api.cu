@@ -10,6 +10,7 @@
 
 #include "ssb_device.cuh"
 #include "ssb_internal.h"
+#include "ssb_redraw.h"
 
 #ifndef SSB_FUSED_BK
 #define SSB_FUSED_BK 16

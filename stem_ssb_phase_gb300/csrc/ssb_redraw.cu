@@ -21,6 +21,7 @@
 
 #include "ssb_device.cuh"
 #include "ssb_internal.h"
+#include "ssb_redraw.h"
 #include "ssb_regfft.cuh"
 
 namespace ssb {
