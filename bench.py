@@ -441,16 +441,11 @@ def run_fit(args):
     ctx.close()
 
 
-def fp32_alu_peak_tflops(sm_mhz: float, sms: int = 152) -> float:
-    """FP32 FMA issue peak on the CUDA cores: 128 lanes per SM, 2 flops per FMA."""
-    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
-
-
-def upsample_flops(n: int, factor: int) -> float:
-    """Real flops of the two complex interpolation products T = O A^T (N x fN x N) and
-    O_up = A T (fN x fN x N), 8 per complex multiply-add."""
+def upsample_algorithmic_bytes(n: int, factor: int, want_object: bool = True) -> int:
+    """Bytes the interpolation must move once: the float64 object accumulator in, the
+    (f N)^2 float32 phase and complex64 object out."""
     fn = factor * n
-    return 8.0 * (n * n * fn + fn * fn * n)
+    return n * n * 16 + fn * fn * (4 + (8 if want_object else 0))
 
 
 def redraw_algorithmic_bytes(n_bf: int, n: int) -> int:
@@ -462,8 +457,8 @@ def run_upsample(args):
     """Object redraw at the benchmark trial, on the device, through the C ABI.
 
     --upsample F: ssb_reconstruct_upsampled, the objective (with the native loss) and the
-    object sum in one pass, then the band-limited interpolation (roofline of the two
-    k_upsample launches against the FP32 FMA issue peak).
+    object sum in one pass, then the band-limited interpolation (HBM roofline of the
+    interpolation kernels, k_up_*: its input and output bytes over their live time).
     --redraw F: ssb_redraw, the phase-of-mean without the loss, from the spectral sum
     over the BF pixels and one 2-D inverse transform (roofline of k_redraw_sum, which
     reads the G cache once, against the measured HBM bandwidth), then the interpolation
@@ -517,7 +512,7 @@ def run_upsample(args):
         prof = ssbgpu.profile_end()
     clk = clocks.stop()
     per = {k: t / args.steps for k, (c, t) in sorted(prof.items())}
-    up_ms = sum(t for k, t in per.items() if k.startswith("k_upsample"))
+    up_ms = sum(t for k, t in per.items() if k.startswith("k_up_"))
     sm_mhz = clk["sm_mhz"] if clk else 2070.0
     hbm, kind = _peaks()
     if phase_only:
@@ -530,11 +525,12 @@ def run_upsample(args):
                 "peak_kind": "%s hbm_gbs (copy)" % kind}
         metric = "phase-of-mean redraw without the loss (spectral sum + one 2-D inverse transform), ms per redraw"
     else:
-        peak = fp32_alu_peak_tflops(sm_mhz)
-        achieved = upsample_flops(n, f) / (up_ms * 1e-3) / 1e12 if up_ms > 0 else None
-        roof = {"bound": "alu", "kernel": "k_upsample", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak if achieved else None, "traffic": None,
-                "peak_basis": "FP32 FMA issue, 152 SMs x 128 lanes x 2 at the median SM clock"}
+        ubytes = upsample_algorithmic_bytes(n, f)
+        achieved = ubytes / 1e9 / (up_ms * 1e-3) if up_ms > 0 else None
+        roof = {"bound": "hbm", "kernel": "k_up_fwd + k_up_cols + k_up_rows", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm if achieved else None,
+                "traffic": None, "algorithmic_bytes_per_launch": ubytes,
+                "peak_kind": "%s hbm_gbs (copy)" % kind}
         metric = "upsampled object redraw (objective + band-limited interpolation), ms per redraw"
     res = {"metric": metric, "value": ms, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
            "steps": args.steps, "warmup": args.warmup, "dtype": "f32", "data": "synthetic",

@@ -85,8 +85,8 @@ cudaError_t launch_finalize(const ObjectiveArgs &a, float *mean_phase, float *ou
                             cudaStream_t s);
 
 // ---- upsampled redraw (ssb_upsample.cu) ----
-// Interpolation table a(d), d = -factor (N - 1) .. factor N - 1 (complex64), and the size
-// of the intermediate T = O A^T (N x factor N complex64).
+// Twist table exp(2 pi i m / (factor N)), m < factor N (complex64), and the size of the
+// transform scratch (factor + 2 planes of N x N complex64).
 size_t upsample_table_elems(int N, int factor);
 size_t upsample_scratch_elems(int N, int factor);
 void upsample_table(int N, int factor, std::vector<float2> &tab);

@@ -149,7 +149,7 @@ def test_profiling_session_times_the_redraw(ssbgpu, tiny_data):
         ssbgpu.profile_begin()  # one session per thread
     ctx.redraw(w.truth, 2)
     prof = ssbgpu.profile_end()
-    for k in ("k_redraw_sum", "k_redraw_combine", "k_redraw_fft", "k_upsample_rows", "k_upsample_cols"):
+    for k in ("k_redraw_sum", "k_redraw_combine", "k_redraw_fft", "k_up_fwd", "k_up_cols", "k_up_rows"):
         assert k in prof and prof[k][1] > 0.0, (k, prof)
     assert prof["k_redraw_fft"][0] == 2
     with pytest.raises(ssbgpu.SSBError):
