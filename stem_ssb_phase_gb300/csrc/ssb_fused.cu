@@ -121,7 +121,9 @@ struct FusedShape {
                                         : OFF_RFFT + (GROUPS * SMR + 1) / 2 * 2;
     static constexpr int TILEBUF = SSB1 ? H * LDC : H * LDC + LDZ + M;  // segments (, h, Rp)
     static constexpr int U_COL = GROUPS * SMF;
-    static constexpr int U_ROW = OFF_TILE - OFF_U + 2 * TILEBUF;
+    // cp.async tiles are triple-buffered (one block barrier per plane), tensor-copy tiles
+    // double-buffered
+    static constexpr int U_ROW = OFF_TILE - OFF_U + (TMA ? 2 : 3) * TILEBUF;
     // + 128 float2 so that the tiles can be placed on a 1024-byte boundary at run time
     static constexpr int TOTAL = OFF_U + (U_COL > U_ROW ? U_COL : U_ROW) + (TMA ? 128 : 0);
     static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float2);
@@ -433,25 +435,28 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         if (tid == 0) row_issue_tma<N, SSB1>(p, map, slot, 0, ry0, tiles, bars);
     } else {
         row_issue<N, SSB1>(p, slot, 0, ry0, tiles);
+        if (planes > 1) row_issue<N, SSB1>(p, slot, 1, ry0, tiles + S::TILEBUF);
     }
     for (int kk = 0; kk < planes; ++kk) {
-        const int buf = kk & 1;
+        const int buf = S::TMA ? (kk & 1) : kk % 3;
         float2 *cur = tiles + buf * S::TILEBUF;
-        __syncthreads();  // everyone is done with the other buffer (plane kk - 1)
         if (S::TMA) {
+            __syncthreads();  // everyone is done with the other buffer (plane kk - 1)
             if (tid == 0 && kk + 1 < planes)
                 row_issue_tma<N, SSB1>(p, map, slot, kk + 1, ry0, tiles + (buf ^ 1) * S::TILEBUF,
                                        bars + 8u * (buf ^ 1));
             mbar_wait(bars + 8u * buf, (tphase >> buf) & 1u, err);  // plane kk has landed
             tphase ^= 1u << buf;
         } else {
-            if (kk + 1 < planes) {
-                row_issue<N, SSB1>(p, slot, kk + 1, ry0, tiles + (buf ^ 1) * S::TILEBUF);
+            // planes kk and kk + 1 are in flight; the barrier publishes plane kk to the block
+            // and frees the buffer of plane kk - 1, which then receives plane kk + 2
+            if (kk + 1 < planes)
                 cp_async_wait<1>();
-            } else {
+            else
                 cp_async_wait<0>();
-            }
-            __syncthreads();  // plane kk has landed for every thread
+            __syncthreads();
+            if (kk + 2 < planes)
+                row_issue<N, SSB1>(p, slot, kk + 2, ry0, tiles + ((kk + 2) % 3) * S::TILEBUF);
         }
         if (tid == 0) {
             // This task no longer needs plane kk of the slot: columns of batch b + D may
