@@ -83,3 +83,13 @@ def test_source_digest_covers_the_fused_kernels_translation_unit():
     import bench
     tu = bench.kernel_includes(os.path.join(ROOT, "stem_ssb_phase_gb300", "csrc", "ssb_fused.cu"))
     assert sorted(os.path.relpath(f, ROOT) for f in tu) == sorted(bench.KERNEL_SOURCES)
+
+
+def test_redraw_and_upsample_byte_counts():
+    """The algorithmic bytes the redraw and interpolation rooflines divide by."""
+    import bench
+    # G cache of the full workload: 8,937 planes of 257 x 512 complex64
+    assert bench.redraw_algorithmic_bytes(8937, 512) == 9_407_729_664
+    # interpolation at f = 4: float64 accumulator in, 2048^2 float32 phase + complex64 out
+    assert bench.upsample_algorithmic_bytes(512, 4) == 512 * 512 * 16 + 2048 * 2048 * 12
+    assert bench.upsample_algorithmic_bytes(512, 1, want_object=False) == 512 * 512 * 20
