@@ -242,7 +242,8 @@ def run_ours(args, rank, world, local_rank):
     cores = len(os.sched_getaffinity(0))
     sample = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = counts[: min(geom.n_bf, 16 * cores * 4)].cpu().numpy()
+        # enough BF planes for about 15 s of oracle work on all host cores (sized below)
+        sample = counts[: min(geom.n_bf, 16 * cores * 16)].cpu().numpy()
         sample = sample.view(np.uint32) if w.dtype == "u32" else sample.view(np.uint16)
     ctx = ssbgpu.SSB(geom, counts, transfer=args.transfer)
     del counts
