@@ -122,8 +122,11 @@ ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phas
  *   phase_out:      device [factor N][factor N] float32, arg of the object  (required)
  *   object_c64_out: device [factor N][factor N] complex64 interleaved        (nullable)
  *   loss_out:       host, one float64                                        (nullable)
- * The context allocates an interpolation table and an N x factor N complex64 intermediate
- * on the first call with a new factor (not counted by ssb_info); SSB_ERR_OOM if that fails. */
+ * The interpolation runs as factor^2 twisted N x N inverse transforms of the object's
+ * spectrum, so any integer factor is exact up to float32 rounding.  The context allocates
+ * a twist table (factor N complex64) and (factor + 2) N^2 complex64 of transform scratch
+ * on the first call with a larger factor (not counted by ssb_info); SSB_ERR_OOM if that
+ * fails. */
 ssb_status ssb_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int factor,
                                      float *phase_out, float *object_c64_out, double *loss_out,
                                      void *cuda_stream);
