@@ -85,6 +85,18 @@ def test_upsampled_object_matches_the_oracle(ssbgpu, tiny_data, small_data, name
     assert np.linalg.norm(sub - o1) <= 1e-5 * np.linalg.norm(o1)
 
 
+@pytest.mark.parametrize("factor", [5, 8])
+def test_large_factors(ssbgpu, tiny_data, factor):
+    """Factors past the pages' 1-4, up to the largest accepted (an odd one and 8)."""
+    w, geom, counts = tiny_data
+    ctx = ssbgpu.SSB(geom, counts)
+    ph, obj, _ = ctx.reconstruct_upsampled(w.truth, factor)
+    ref = oracle.objective(geom, w.truth, counts=counts, want_object=True)
+    check_upsampled(ph.cpu().numpy(), obj.cpu().numpy(), ref["object"], factor)
+    ph2, obj2 = ctx.redraw(w.truth, factor)
+    check_upsampled(ph2.cpu().numpy(), obj2.cpu().numpy(), ref["object"], factor)
+
+
 def test_ssb1_upsampled_object(ssbgpu, small_data):
     w, geom, counts = small_data
     ctx = ssbgpu.SSB(geom, counts, transfer="ssb1")
