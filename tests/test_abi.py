@@ -78,3 +78,17 @@ def test_invalid_geometry_is_rejected(lib, field, value):
     out = ctypes.c_void_p()
     assert lib.ssb_prepare(ctypes.byref(g), counts.ctypes.data, 0, 0, 0, None,
                            ctypes.byref(out)) == 1
+
+
+def test_profiling_session_bookkeeping_on_the_host(lib):
+    """A session with no launches needs no device: it opens once per thread, closes with
+    an empty report, and a second close is refused."""
+    ssbgpu.profile_begin()
+    with pytest.raises(ssbgpu.SSBError) as ei:
+        ssbgpu.profile_begin()
+    assert ei.value.status == 1
+    assert lib.ssb_profile_objective(None, None, None, 0, None, None) == 1
+    assert ssbgpu.profile_end() == {}
+    with pytest.raises(ssbgpu.SSBError) as ei:
+        ssbgpu.profile_end()
+    assert ei.value.status == 1
