@@ -185,17 +185,19 @@ ssb_status ssb_profile_end(ssb_kernel_time *out, int cap, int *n_out);
 
 /* Loss of one trial without any device allocation.  (The pages have no counterpart: this
  * entry point exists for callers of this library that cannot allocate device memory when
- * they need a loss -- code running while its stream is captured into a CUDA graph, where
- * cudaMalloc is not allowed, real-time pipelines that forbid allocation after set-up, and
- * plug-ins whose host application owns all GPU memory.)
+ * they need a loss -- real-time pipelines that forbid allocation after set-up, because an
+ * allocation can block on the driver and break their timing, and plug-ins whose host
+ * application owns all GPU memory through its own allocator.)
  *   g:              geometry, as for ssb_prepare (host); transfer is SSB2.
  *   g_cache_device: the G cache on the current device, complex64 [n_bf][N/2+1][N], the
  *                   layout ssb_export_g writes; read only.
  *   theta:          host, one trial.     loss_out: host, one float64.
  * All scratch lives in one static 24 MiB device array that every GPU using the library
  * holds until the process exits; problems that do not fit (n_bf > 16384, or a layout
- * beyond 24 MiB) fail with SSB_ERR_ARG before any device work.  The first call on a device
- * looks up the array's device address; make that first call before any stream capture.
+ * beyond 24 MiB) fail with SSB_ERR_ARG before any device work.  Set-up: the first call on
+ * a device (and the first after that device's context was reset) looks up the array's
+ * device address; make that first call before any stream capture.  *loss_out is written
+ * only when the call returns SSB_OK.
  * Calls share the array and its contents persist between calls (what must start at zero
  * is cleared by each call), so calls that overlap on the GPU -- concurrent streams,
  * threads or devices sharing a call in flight -- race and must be serialised by the

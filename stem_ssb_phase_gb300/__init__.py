@@ -26,6 +26,8 @@ EXPORTS = ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_reconstruct_
            "ssb_unpack_counts", "ssb_profile_objective", "ssb_profile_begin", "ssb_profile_end",
            "ssb_redraw", "ssb_loss_noalloc", "ssb_status_string",
            "ssb_last_error", "ssb_kernel_launches", "ssb_destroy")
+# the test hooks include/ssb_debug.h declares
+DEBUG_EXPORTS = ("ssb_debug_stall_next", "ssb_debug_poison_scratch", "ssb_debug_atan2")
 
 
 class SSBError(RuntimeError):
@@ -86,9 +88,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssb_kernel_launches.restype = ctypes.c_uint64
     lib.ssb_destroy.argtypes = [vp]
     lib.ssb_destroy.restype = None
+    lib.ssb_debug_stall_next.argtypes = [vp, i, ctypes.c_uint]
+    lib.ssb_debug_poison_scratch.argtypes = [vp, vp]
+    lib.ssb_debug_atan2.argtypes = [vp, vp, sz, vp, vp]
     for name in ("ssb_prepare", "ssb_loss_batch", "ssb_reconstruct", "ssb_reconstruct_upsampled", "ssb_info",
                  "ssb_export_g", "ssb_unpack_counts", "ssb_profile_objective",
-                 "ssb_profile_begin", "ssb_profile_end", "ssb_redraw", "ssb_loss_noalloc"):
+                 "ssb_profile_begin", "ssb_profile_end", "ssb_redraw", "ssb_loss_noalloc") + DEBUG_EXPORTS:
         getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -243,6 +248,18 @@ class SSB:
                                     _stream_handle(stream)), "ssb_redraw")
         return ph, obj
 
+    # ------------------------------------------------------------------ test hooks
+    def debug_stall_next(self, evaluation: int, polls: int):
+        """Make evaluation `evaluation` of the next objective call stall its row tasks on a
+        count nothing reaches, giving up after `polls` polls (ssb_debug.h)."""
+        _check(self._lib.ssb_debug_stall_next(self._ctx, int(evaluation), int(polls)),
+               "ssb_debug_stall_next")
+
+    def debug_poison_scratch(self, stream=None):
+        """Fill every per-evaluation scratch buffer with 0xFF bytes (NaN) (ssb_debug.h)."""
+        _check(self._lib.ssb_debug_poison_scratch(self._ctx, _stream_handle(stream)),
+               "ssb_debug_poison_scratch")
+
     def export_g(self, stream=None):
         """The G cache as a CUDA complex64 tensor [n_bf][N/2+1][N] (Qx-major, Qy contiguous)."""
         import torch
@@ -294,6 +311,19 @@ def unpack_counts(counts, stream=None):
     _check(lib.ssb_unpack_counts(ctypes.c_void_p(src.data_ptr()), dt, src.numel(),
                                  ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)),
            "ssb_unpack_counts")
+    return out
+
+
+def debug_atan2(y, x, stream=None):
+    """The objective's float32 phase function atan2(y, x) on CUDA float32 tensors."""
+    import torch
+    yc, xc = y.contiguous(), x.contiguous()
+    if yc.dtype != torch.float32 or xc.dtype != torch.float32 or yc.shape != xc.shape:
+        raise TypeError("y and x must be float32 CUDA tensors of one shape")
+    out = torch.empty_like(yc)
+    _check(load_library().ssb_debug_atan2(ctypes.c_void_p(yc.data_ptr()), ctypes.c_void_p(xc.data_ptr()),
+                                          yc.numel(), ctypes.c_void_p(out.data_ptr()),
+                                          _stream_handle(stream)), "ssb_debug_atan2")
     return out
 
 

@@ -8,6 +8,7 @@
 #include <string>
 #include <vector>
 
+#include "../../include/ssb_debug.h"
 #include "ssb_device.cuh"
 #include "ssb_internal.h"
 #include "ssb_redraw.h"
@@ -118,6 +119,10 @@ struct ssb_ctx {
     // redraw-without-loss scratch, allocated on first use
     double2 *rd_part = nullptr;
     float2 *rd_S = nullptr, *rd_T = nullptr;
+    // test hook (ssb_debug_stall_next): the evaluation with this index in the next call
+    // stalls its row tasks on a count that is never reached, with this poll limit
+    int dbg_stall_eval = -1;
+    unsigned dbg_wait_limit = 0;
 
     ObjectiveArgs args() const {
         ObjectiveArgs a;
@@ -144,6 +149,8 @@ struct ssb_ctx {
         a.lam = lam;
         a.semi = semi;
         a.dalpha = dalpha;
+        a.wait_limit = 0;
+        a.stall = 0;
         return a;
     }
 };
@@ -160,15 +167,31 @@ static void free_ctx(ssb_ctx *c) {
 
 static bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
 
+// Evaluation number `index` of the current library call (the stall test hook applies to one).
 static cudaError_t evaluate(const ssb_ctx *c, const ssb_params &theta, double *loss_slot,
-                            bool want_object, cudaStream_t s) {
-    return run_objective_fused(c->args(), theta, loss_slot, want_object, s);
+                            bool want_object, cudaStream_t s, int index = 0) {
+    ObjectiveArgs a = c->args();
+    if (index == c->dbg_stall_eval) {
+        a.stall = 1;
+        a.wait_limit = c->dbg_wait_limit;
+    }
+    return run_objective_fused(a, theta, loss_slot, want_object, s);
 }
 
-// After an evaluation: the scheduler's error word (a bounded wait that ran out).
-static ssb_status check_sync(const ssb_ctx *c, cudaStream_t s) {
+// Start of a library call that evaluates the objective: clear the scheduler's error word
+// (it stays raised for the rest of the call once a wait has run out).
+static ssb_status begin_call(const ssb_ctx *c, cudaStream_t s) {
+    SSB_CK(cudaMemsetAsync(c->sync, 0, sizeof(unsigned), s));
+    return SSB_OK;
+}
+
+// End of such a call: the scheduler's error word (a bounded wait that ran out in any of
+// the call's evaluations); consumes the stall test hook.
+static ssb_status check_sync(ssb_ctx *c, cudaStream_t s) {
+    c->dbg_stall_eval = -1;
+    c->dbg_wait_limit = 0;
     unsigned h = 0;
-    SSB_CK(cudaMemcpyAsync(&h, c->sync + 1, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+    SSB_CK(cudaMemcpyAsync(&h, c->sync, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
     SSB_CK(cudaStreamSynchronize(s));
     if (h) return fail(SSB_ERR_TIMEOUT, "a scheduler wait in the fused objective kernel ran out");
     return SSB_OK;
@@ -385,17 +408,18 @@ ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *lo
     DeviceGuard dg(c->dev);
     if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
     cudaStream_t s = (cudaStream_t)cuda_stream;
-    const ObjectiveArgs a = c->args();
+    ssb_status st = begin_call(c, s);
+    if (st != SSB_OK) return st;
     for (int t0 = 0; t0 < T; t0 += c->loss_cap) {
         const int tn = std::min(c->loss_cap, T - t0);
         for (int t = 0; t < tn; ++t) {
-            cudaError_t e = evaluate(c, theta[t0 + t], c->loss + t, false, s);
+            cudaError_t e = evaluate(c, theta[t0 + t], c->loss + t, false, s, t0 + t);
             if (e != cudaSuccess) return cuda_fail(e, "objective launch");
         }
         SSB_CK(cudaMemcpyAsync(loss_out + t0, c->loss, sizeof(double) * tn, cudaMemcpyDeviceToHost, s));
-        SSB_CK(cudaStreamSynchronize(s));
-        ssb_status st = check_sync(c, s);
-        if (st != SSB_OK) return st;
+        // the error word is cleared once per call, so this sees a wait that ran out in any
+        // trial so far (those trials and all later ones have NaN losses)
+        if ((st = check_sync(c, s)) != SSB_OK) return st;
     }
     return SSB_OK;
 }
@@ -409,6 +433,8 @@ ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phas
     if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
     cudaStream_t s = (cudaStream_t)cuda_stream;
     const ObjectiveArgs a = c->args();
+    ssb_status st = begin_call(c, s);
+    if (st != SSB_OK) return st;
     cudaError_t e = evaluate(c, *theta, c->loss, object_c64_out != nullptr, s);
     if (e != cudaSuccess) return cuda_fail(e, "objective launch");
     if ((e = launch_finalize(a, mean_phase_out, object_c64_out, s)) != cudaSuccess)
@@ -479,6 +505,7 @@ ssb_status ssb_reconstruct_upsampled(ssb_ctx *c, const ssb_params *theta, int fa
     cudaStream_t s = (cudaStream_t)cuda_stream;
     ssb_status st = ensure_upsample(c, factor, s);
     if (st != SSB_OK) return st;
+    if ((st = begin_call(c, s)) != SSB_OK) return st;
     const ObjectiveArgs a = c->args();
     cudaError_t e = evaluate(c, *theta, c->loss, true, s);
     if (e != cudaSuccess) return cuda_fail(e, "objective launch");
@@ -554,11 +581,14 @@ ssb_status ssb_profile_objective(ssb_ctx *c, const ssb_params *theta, ssb_kernel
     if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
     cudaStream_t s = (cudaStream_t)cuda_stream;
     if (g_prof) return fail(SSB_ERR_ARG, "a profiling session is open on this thread");
+    ssb_status st = begin_call(c, s);
+    if (st != SSB_OK) return st;
     Profiler prof;
     g_prof = &prof;
     cudaError_t e = evaluate(c, *theta, c->loss, false, s);
     g_prof = nullptr;
-    return collect_profile(prof, e, out, cap, n_out, "profiled objective");
+    if ((st = collect_profile(prof, e, out, cap, n_out, "profiled objective")) != SSB_OK) return st;
+    return check_sync(c, s);
 }
 
 static thread_local Profiler *g_session = nullptr;
@@ -629,6 +659,43 @@ ssb_status ssb_unpack_counts(const void *in_device, ssb_dtype dtype, size_t n, f
     cudaFree(flag);
     if (e != cudaSuccess) return cuda_fail(e, "unpack");
     if (h & 1) return fail(SSB_ERR_ARG, "a count exceeds 2^24 and cannot be converted to float32 exactly");
+    return SSB_OK;
+}
+
+ssb_status ssb_debug_stall_next(ssb_ctx *c, int evaluation, unsigned polls) {
+    g_last_error.clear();
+    if (!c) return fail(SSB_ERR_ARG, "NULL context");
+    if (evaluation < 0) return fail(SSB_ERR_ARG, "evaluation must be >= 0");
+    c->dbg_stall_eval = evaluation;
+    c->dbg_wait_limit = polls ? polls : 1u;
+    return SSB_OK;
+}
+
+ssb_status ssb_debug_poison_scratch(ssb_ctx *c, void *cuda_stream) {
+    g_last_error.clear();
+    if (!c) return fail(SSB_ERR_ARG, "NULL context");
+    DeviceGuard dg(c->dev);
+    if (!dg.ok) return fail(SSB_ERR_CUDA, "cannot select the context's device");
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    const size_t P = (size_t)c->N * c->N;
+    const bool ssb1 = c->transfer == SSB_TRANSFER_SSB1;
+    struct Buf {
+        void *p;
+        size_t bytes;
+    } bufs[] = {
+        {c->Zring, fused_ring_elems(c->N, c->Bk, c->D, ssb1) * sizeof(float2)},
+        {c->hring, fused_hring_elems(c->N, c->Bk, c->D) * sizeof(float2)},
+        {c->rring, fused_rring_elems(c->N, c->Bk, c->D) * sizeof(float2)},
+        {c->S2g, fused_s2g_elems(c->N) * sizeof(double)},
+        {c->sync, fused_sync_words(c->N, c->n_bf, c->Bk) * sizeof(unsigned)},
+        {c->S1, P * sizeof(double)},
+        {c->Osum, P * sizeof(double2)},
+        {c->E, P * sizeof(float2)},
+        {c->kturn, (size_t)c->n_bf * sizeof(uint2)},
+        {c->loss, (size_t)c->loss_cap * sizeof(double)},
+    };
+    for (const Buf &b : bufs) SSB_CK(cudaMemsetAsync(b.p, 0xff, b.bytes, s));
+    SSB_CK(cudaStreamSynchronize(s));
     return SSB_OK;
 }
 

@@ -8,6 +8,34 @@
 
 namespace ssb {
 
+// Per-pixel phase sums S1 (8 bytes per pixel): float64, or with SSB_S1_DF a pair of floats
+// hi + lo updated by an exact two-sum (about 48 significant bits, no float64 arithmetic).
+#ifndef SSB_S1_DF
+#define SSB_S1_DF 0
+#endif
+#ifndef SSB_ATAN_FLOOR
+#define SSB_ATAN_FLOOR 0
+#endif
+
+// s = (hi, lo) += v: hi takes the float32 sum, lo the exact rounding error of that sum
+// (Knuth's two-sum, six additions, valid for any magnitudes).
+__device__ __forceinline__ float2 df_add(float2 s, float v) {
+    const float hi = s.x + v;
+    const float bv = hi - s.x;
+    const float err = (s.x - (hi - bv)) + (v - bv);
+    return make_float2(hi, s.y + err);
+}
+
+// S1 of pixel i as a float64 value
+__device__ __forceinline__ double s1_value(const double *S1, int i) {
+#if SSB_S1_DF
+    const float2 e = reinterpret_cast<const float2 *>(S1)[i];
+    return (double)e.x + (double)e.y;
+#else
+    return S1[i];
+#endif
+}
+
 __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
     return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.x, b.y, a.y * b.x));
 }
@@ -207,7 +235,11 @@ __device__ __forceinline__ float2 correct_ssb1(float2 g, float fsy, int sy, floa
 __device__ __forceinline__ float fast_atan2(float y, float x) {
     const float ax = fabsf(x), ay = fabsf(y);
     const float mx = fmaxf(ax, ay), mn = fminf(ax, ay);
+#if SSB_ATAN_FLOOR
+    const float a = __fdividef(mn, fmaxf(mx, 1.17549435e-38f));  // 0/0 -> 0 without a branch
+#else
     const float a = mx > 0.0f ? __fdividef(mn, mx) : 0.0f;
+#endif
     const float s = a * a;
     float p = -4.054552875e-03f;
     p = fmaf(p, s, 2.186291292e-02f);

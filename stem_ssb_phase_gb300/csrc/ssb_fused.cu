@@ -70,10 +70,12 @@ struct FusedParams {
     double *S1;           // [P]
     double *S2g;          // [row tasks]
     double2 *Osum;        // [P] (object redraw only)
-    unsigned *sync;       // ticket, error, col_done[nbatch], plane_free[nbatch][Bk],
+    unsigned *sync;       // error, ticket, col_done[nbatch], plane_free[nbatch][Bk],
                           // h_cnt[nbatch][Bk], chain[row tasks]
     int n_bf, Bk, nbatch;
     int D;                // ring slots (batches in flight)
+    unsigned wait_limit;  // polls before a wait gives up (kWaitLimit unless a test lowers it)
+    int stall;            // test hook: row tasks wait for a count that is never reached
     TrialConst tc;
 };
 
@@ -87,9 +89,13 @@ struct FusedShape {
     static constexpr int H = SSB1 ? N : N / 2 + 1;  // columns corrected and column-transformed
     static constexpr int M = SSB1 ? N : N / 2;      // row transform length
     static constexpr int RE = SSB1 ? kPts : 8;      // row transform points per thread (M / T)
+    // Column tasks cover HC columns per plane; the SSB2 column N/2 is transformed by the
+    // task that completes the plane (beside the Nyquist-row term), so that for N = 512 the
+    // 256 task columns split evenly into tasks.
+    static constexpr int HC = SSB1 ? N : N / 2;
     static constexpr int CW = GROUPS * kColsPerWarp;  // columns per column task
     static constexpr int RT = GROUPS < N ? GROUPS : N;  // rows per row task (multiple of 4)
-    static constexpr int CT = (H + CW - 1) / CW;    // column tasks per plane
+    static constexpr int CT = (HC + CW - 1) / CW;   // column tasks per plane
     static constexpr int NR = N / RT;               // row tasks per trial
     static constexpr int SMF = RegFFT<N, kPts>::SMEM;  // FFT scratch per group
     static constexpr int LDZ = (N / 2 + 1 + 7) / 8 * 8;  // h row stride (64 B multiple)
@@ -191,11 +197,12 @@ __device__ __forceinline__ void st_relaxed(unsigned *p, unsigned v) {
 
 // Called by one thread: wait until *addr >= target.  Returns false if the wait gave up
 // (error flag already raised elsewhere, or the poll budget ran out, which raises it).
-__device__ bool wait_at_least(const unsigned *addr, unsigned target, unsigned *err) {
+__device__ bool wait_at_least(const unsigned *addr, unsigned target, unsigned *err,
+                              unsigned limit) {
     unsigned polls = 0;
     while (ld_acquire(addr) < target) {
         if (ld_acquire(err) != 0u) return false;
-        if (++polls > kWaitLimit) {
+        if (++polls > limit) {
             atomicOr(err, 2u);
             return false;
         }
@@ -248,19 +255,108 @@ __device__ void nyquist_transform(const FusedParams &p, float2 *fsm, const float
     }
 }
 
-// One column task.  free_word (NULL on the slot's first use) counts the row tasks of batch
+// One transformed column: column nx of BF plane k (plane kk of ring slot `slot`), by the
+// calling thread's transform group (thread j of T).  Loads G and E, applies the correction,
+// runs the column IFFT and leaves the result in v; for SSB2 also the Nyquist-row Hermitian
+// part h(nx) of the mirror bin (hstore: this thread stores hval).  Groups with valid =
+// false transform zeros.  Columns with exactly zero transfer (SSB2: both shifted
+// apertures miss the whole column; SSB1: the aperture at alpha_k - lambda Q' does; every
+// column but DC for an inactive BF pixel) skip the loads, the correction and the
+// transform: the decision is uniform over the warp, and v is then zero.  Every lane of the
+// warp must call it (the transform synchronises the warp).
+// SSB1 column nx > N/2 reads the cache's column N - nx at the mirrored rows, conjugated
+// (G(-Q) = conj G(Q)).
+template <int N, bool SSB1>
+__device__ __forceinline__ void column_compute(const FusedParams &p, float2 *smem, int k, int nx,
+                                               bool valid, const float4 &geo, const uint2 &bt,
+                                               float2 (&v)[kPts], float2 &hval, bool &hstore) {
+    using S = FusedShape<N, SSB1>;
+    constexpr int HG = N / 2 + 1;  // columns of the half-plane G cache
+    const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
+    const int sx = nx < N / 2 ? nx : nx - N;
+    const bool zero = nx > 0 && (!(geo.z > 0.0f) || (SSB1 ? column_zero1(sx, geo.x, geo.y, p.tc)
+                                                           : column_zero(sx, geo.x, geo.y, p.tc)));
+    const bool skip = __all_sync(0xffffffffu, zero || !valid);
+    hval = make_float2(0.f, 0.f);
+    hstore = !SSB1 && valid && skip && j == 0 && nx >= 1 && nx < N / 2;  // h = 0 there
+    if (valid && !skip) {
+        const float2 *e = p.Et + (size_t)nx * N + j;
+        float2 ev[kPts];
+        if (!SSB1 || nx <= N / 2) {
+            const float2 *g = p.G + ((size_t)k * HG + nx) * N + j;
+#pragma unroll
+            for (int r = 0; r < kPts; ++r) v[r] = __ldcs(g + S::T * r);
+        } else {  // G(ny, nx) = conj G(N - ny, N - nx), row indices mod N
+            const float2 *g = p.G + ((size_t)k * HG + (N - nx)) * N;
+#pragma unroll
+            for (int r = 0; r < kPts; ++r) v[r] = cconj(__ldcs(g + ((N - j - S::T * r) & (N - 1))));
+        }
+#pragma unroll
+        for (int r = 0; r < kPts; ++r) ev[r] = __ldg(e + S::T * r);
+        const ColGeom cg = col_geom(sx, geo.x, geo.y, p.tc);
+        const float fj = (float)j;
+        const uint32_t phx = bt.x * (uint32_t)sx;
+        const bool active = geo.z > 0.0f;  // a(alpha_k) = 0: only the DC term survives
+#pragma unroll
+        for (int r = 0; r < kPts; ++r) {
+            const int ny = j + S::T * r;
+            // signed bin: ny for r < kPts/2 (ny < N/2), ny - N above
+            const int off = S::T * r - (r >= kPts / 2 ? N : 0);
+            const int sy = j + off;
+            const float fsy = fj + (float)off;
+            const float2 gv = v[r];
+            float2 cv = make_float2(0.f, 0.f);
+            if (active)
+                cv = SSB1 ? correct_ssb1(gv, fsy, sy, ev[r], cg, phx, bt.y, p.tc)
+                          : correct_ssb2(gv, fsy, sy, ev[r], cg, phx, bt.y, p.tc);
+            if ((nx | ny) == 0) cv = gv;  // C(0) = G(0)
+            if (!SSB1 && r == kPts / 2 && j == 0 && nx >= 1 && nx < N / 2) {
+                // Nyquist row (ny = N/2): the mirror bin N - nx has no partner and
+                // carries its own correction, at signed bins (-nx, -N/2), where the
+                // column geometry has p0 negated
+                const float2 em = __ldg(p.Et + (size_t)(N - nx) * N + N / 2);
+                ColGeom cm = cg;
+                cm.p0 = -cg.p0;
+                const float2 c2 = active ? correct_ssb2(cconj(gv), -(float)(N / 2), -N / 2, em, cm,
+                                                         0u - phx, bt.y, p.tc)
+                                         : make_float2(0.f, 0.f);
+                hval = make_float2(0.5f * (cv.x + c2.x), 0.5f * (cv.y - c2.y));
+                hstore = true;
+            }
+            v[r] = cv;
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < kPts; ++r) v[r] = make_float2(0.f, 0.f);
+    }
+    if (!skip)
+        reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
+}
+
+// Store a transformed column into its ring plane (and h(nx), SSB2).
+template <int N, bool SSB1>
+__device__ __forceinline__ void column_store(const FusedParams &p, int slot, int kk, int nx,
+                                             const float2 (&v)[kPts], float2 hval, bool hstore) {
+    using S = FusedShape<N, SSB1>;
+    const int j = threadIdx.x % S::T;
+    float2 *z = p.Z + (((size_t)slot * p.Bk + kk) * S::H + nx) * N + j;
+#pragma unroll
+    for (int r = 0; r < kPts; ++r) __stcg(z + S::T * r, v[r]);
+    if (hstore) __stcg(p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ + nx, hval);
+}
+
+// One column task: CW of the plane's HC task columns (SSB2: 0 .. N/2 - 1, the task that
+// completes the plane then adds column N/2; SSB1: all N), kColsPerWarp per transform
+// group in turn.  free_word (NULL on the slot's first use) counts the row tasks of batch
 // b - D that have released this plane of the ring slot; the task overwrites the plane only
 // once all of them have.  Each warp reads the count when the task starts and checks it
 // before its first ring write, so the load's latency hides behind the column work.
 // Returns, uniform over the warp, whether the warp could write the slot.
-// SSB1 covers all N columns; column nx > N/2 reads the cache's column N - nx at the
-// mirrored rows, conjugated (G(-Q) = conj G(Q)).
 template <int N, bool SSB1>
 __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
                            const unsigned *free_word, unsigned *err) {
     using S = FusedShape<N, SSB1>;
-    constexpr int HG = N / 2 + 1;  // columns of the half-plane G cache
-    const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T, lane = tid & 31;
+    const int tid = threadIdx.x, grp = tid / S::T, lane = tid & 31;
     const int kk = idx / S::CT, ct = idx - kk * S::CT;
     const int k = b * p.Bk + kk;
     const int slot = b % p.D;
@@ -272,84 +368,37 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
 #pragma unroll 1
     for (int c = 0; c < kColsPerWarp; ++c) {
         const int nx = ct * S::CW + c * S::GROUPS + grp;
-        const bool valid = nx < S::H;
-        const int sx = nx < N / 2 ? nx : nx - N;
-        // Columns with exactly zero transfer (SSB2: both shifted apertures miss the whole
-        // column; SSB1: the aperture at alpha_k - lambda Q' does; every column but DC for an
-        // inactive BF pixel) skip the loads, the correction and the transform and store
-        // zeros.  The decision is uniform over the warp.
-        const bool zero = nx > 0 && (!(geo.z > 0.0f) || (SSB1 ? column_zero1(sx, geo.x, geo.y, p.tc)
-                                                               : column_zero(sx, geo.x, geo.y, p.tc)));
-        const bool skip = __all_sync(0xffffffffu, zero || !valid);
+        const bool valid = nx < S::HC;
         float2 v[kPts];
-        float2 hval = make_float2(0.f, 0.f);
-        bool hstore = !SSB1 && skip && j == 0 && nx >= 1 && nx < N / 2;  // h = 0 there
-        if (valid && !skip) {
-            const float2 *e = p.Et + (size_t)nx * N + j;
-            float2 ev[kPts];
-            if (!SSB1 || nx <= N / 2) {
-                const float2 *g = p.G + ((size_t)k * HG + nx) * N + j;
-#pragma unroll
-                for (int r = 0; r < kPts; ++r) v[r] = __ldcs(g + S::T * r);
-            } else {  // G(ny, nx) = conj G(N - ny, N - nx), row indices mod N
-                const float2 *g = p.G + ((size_t)k * HG + (N - nx)) * N;
-#pragma unroll
-                for (int r = 0; r < kPts; ++r) v[r] = cconj(__ldcs(g + ((N - j - S::T * r) & (N - 1))));
-            }
-#pragma unroll
-            for (int r = 0; r < kPts; ++r) ev[r] = __ldg(e + S::T * r);
-            const ColGeom cg = col_geom(sx, geo.x, geo.y, p.tc);
-            const float fj = (float)j;
-            const uint32_t phx = bt.x * (uint32_t)sx;
-            const bool active = geo.z > 0.0f;  // a(alpha_k) = 0: only the DC term survives
-#pragma unroll
-            for (int r = 0; r < kPts; ++r) {
-                const int ny = j + S::T * r;
-                // signed bin: ny for r < kPts/2 (ny < N/2), ny - N above
-                const int off = S::T * r - (r >= kPts / 2 ? N : 0);
-                const int sy = j + off;
-                const float fsy = fj + (float)off;
-                const float2 gv = v[r];
-                float2 cv = make_float2(0.f, 0.f);
-                if (active)
-                    cv = SSB1 ? correct_ssb1(gv, fsy, sy, ev[r], cg, phx, bt.y, p.tc)
-                              : correct_ssb2(gv, fsy, sy, ev[r], cg, phx, bt.y, p.tc);
-                if ((nx | ny) == 0) cv = gv;  // C(0) = G(0)
-                if (!SSB1 && r == kPts / 2 && j == 0 && nx >= 1 && nx < N / 2) {
-                    // Nyquist row (ny = N/2): the mirror bin N - nx has no partner and
-                    // carries its own correction, at signed bins (-nx, -N/2), where the
-                    // column geometry has p0 negated
-                    const float2 em = __ldg(p.Et + (size_t)(N - nx) * N + N / 2);
-                    ColGeom cm = cg;
-                    cm.p0 = -cg.p0;
-                    const float2 c2 = active ? correct_ssb2(cconj(gv), -(float)(N / 2), -N / 2, em, cm,
-                                                             0u - phx, bt.y, p.tc)
-                                             : make_float2(0.f, 0.f);
-                    hval = make_float2(0.5f * (cv.x + c2.x), 0.5f * (cv.y - c2.y));
-                    hstore = true;
-                }
-                v[r] = cv;
-            }
-        } else {
-#pragma unroll
-            for (int r = 0; r < kPts; ++r) v[r] = make_float2(0.f, 0.f);
-        }
-        if (!skip)
-            reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
+        float2 hval;
+        bool hstore;
+        column_compute<N, SSB1>(p, smem, k, nx, valid, geo, bt, v, hval, hstore);
         if (c == 0) {
             if (lane == 0 && freed < (unsigned)S::NR)
-                ok = wait_at_least(free_word, (unsigned)S::NR, err);
+                ok = wait_at_least(free_word, (unsigned)S::NR, err, p.wait_limit);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             __syncwarp();  // the warp's ring writes follow lane 0's acquire
         }
-        if (valid && ok) {
-            float2 *z = p.Z + (((size_t)slot * p.Bk + kk) * S::H + nx) * N + j;
-#pragma unroll
-            for (int r = 0; r < kPts; ++r) __stcg(z + S::T * r, v[r]);
-            if (hstore) __stcg(p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ + nx, hval);
-        }
+        if (valid && ok) column_store<N, SSB1>(p, slot, kk, nx, v, hval, hstore);
     }
     return ok;
+}
+
+// The SSB2 column N/2 of plane kk (ring slot `slot`) of batch b, by one warp (its first
+// transform group stores), in the task that completes the plane's column pass.  The warp
+// already waited for the plane to be free in that task (ok).
+template <int N>
+__device__ void half_column(const FusedParams &p, float2 *smem, int b, int kk) {
+    using S = FusedShape<N, false>;
+    const int k = b * p.Bk + kk;
+    const float4 geo = __ldg(p.kgeo + k);
+    const uint2 bt = __ldg(p.kturn + k);
+    const bool first = (threadIdx.x & 31) < S::T;  // the warp's first group
+    float2 v[kPts];
+    float2 hval;
+    bool hstore;
+    column_compute<N, false>(p, smem, k, N / 2, first, geo, bt, v, hval, hstore);
+    if (first) column_store<N, false>(p, b % p.D, kk, N / 2, v, hval, false);
 }
 
 // ---------------------------------------------------------------- row task
@@ -525,12 +574,23 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
     // Add this batch into the float64 accumulators.  Only this update is ordered: it
     // waits until the previous batch's task for the same rows has made its own update,
     // which keeps the per-pixel summation order fixed while the tasks themselves overlap.
-    if (tid == 0) *s_ok = wait_at_least(chain + rt, (unsigned)b, err);
+    if (tid == 0) *s_ok = wait_at_least(chain + rt, (unsigned)b, err, p.wait_limit);
     __syncthreads();
     if (SSB1 && active && *s_ok) {
         // pixel j + T r of row ry holds acc1[r]; loads are issued in groups ahead of their
         // stores (a store through the same pointer would hold back each following load)
         constexpr int GS = OBJ ? 4 : 16;
+#if SSB_S1_DF
+        float2 *s1 = reinterpret_cast<float2 *>(p.S1 + (size_t)ry * N) + j;
+#pragma unroll
+        for (int g0 = 0; g0 < 16; g0 += GS) {
+            float2 old[GS];
+#pragma unroll
+            for (int r = 0; r < GS; ++r) old[r] = __ldcg(s1 + S::T * (g0 + r));
+#pragma unroll
+            for (int r = 0; r < GS; ++r) s1[S::T * (g0 + r)] = df_add(old[r], acc1[g0 + r]);
+        }
+#else
         double *s1 = p.S1 + (size_t)ry * N + j;
 #pragma unroll
         for (int g0 = 0; g0 < 16; g0 += GS) {
@@ -540,6 +600,7 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
 #pragma unroll
             for (int r = 0; r < GS; ++r) s1[S::T * (g0 + r)] = old[r] + (double)acc1[g0 + r];
         }
+#endif
         if (OBJ) {
             double2 *os = p.Osum + (size_t)ry * N + j;
 #pragma unroll
@@ -559,6 +620,21 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         // A thread owns pixel pairs (2 (j + T r), 2 (j + T r) + 1).  With the object sums
         // live, smaller groups keep the registers within the launch bound.
         constexpr int GS = OBJ ? 2 : 8;  // S1 pixel pairs per group
+#if SSB_S1_DF
+        float4 *s1 = reinterpret_cast<float4 *>(p.S1 + (size_t)ry * N) + j;
+#pragma unroll
+        for (int g0 = 0; g0 < 8; g0 += GS) {
+            float4 old[GS];
+#pragma unroll
+            for (int r = 0; r < GS; ++r) old[r] = __ldcg(s1 + S::T * (g0 + r));
+#pragma unroll
+            for (int r = 0; r < GS; ++r) {
+                const float2 a = df_add(make_float2(old[r].x, old[r].y), acc1[2 * (g0 + r)]);
+                const float2 c = df_add(make_float2(old[r].z, old[r].w), acc1[2 * (g0 + r) + 1]);
+                s1[S::T * (g0 + r)] = make_float4(a.x, a.y, c.x, c.y);
+            }
+        }
+#else
         double2 *s1 = reinterpret_cast<double2 *>(p.S1 + (size_t)ry * N) + j;
 #pragma unroll
         for (int g0 = 0; g0 < 8; g0 += GS) {
@@ -570,6 +646,7 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
                 s1[S::T * (g0 + r)] = make_double2(old[r].x + (double)acc1[2 * (g0 + r)],
                                                    old[r].y + (double)acc1[2 * (g0 + r) + 1]);
         }
+#endif
         if (OBJ) {
             double2 *os = p.Osum + (size_t)ry * N + 2 * j;  // pixel 2 (j + T r) + e at 2 T r + e
 #pragma unroll
@@ -655,8 +732,8 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
     }
     for (int i = tid; i < N; i += kFusedThreads) smem[S::OFF_TW + lay(i)] = p.tw[i];
     for (int i = tid; i < S::M; i += kFusedThreads) smem[S::OFF_TW2 + lay(i)] = p.tw[2 * i];
-    unsigned *ticket = p.sync;
-    unsigned *err = p.sync + 1;
+    unsigned *err = p.sync;  // cleared once per library call, so a timeout stays raised
+    unsigned *ticket = p.sync + 1;
     unsigned *col_done = p.sync + 2;
     unsigned *plane_free = col_done + p.nbatch;
     unsigned *h_cnt = plane_free + (size_t)p.nbatch * p.Bk;
@@ -694,10 +771,14 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
             }
             __syncthreads();
             if (!SSB1 && s_nyq) {
-                if (tid < 32 && ok)  // whole warp: the transform synchronises the warp
+                // whole warps (the transforms synchronise the warp): warp 0 the Nyquist-row
+                // term, warp 1 the column N/2
+                if (tid < 32 && ok)
                     nyquist_transform<N>(p, smem + S::OFF_FFT + (tid / S::T) * S::SMF,
                                          smem + S::OFF_TW, smem + S::OFF_TW2, task.b % p.D, kk,
                                          tid % S::T, tid < S::T);
+                else if (tid >= 32 && tid < 64 && ok)
+                    half_column<N>(p, smem, task.b, kk);
                 __syncthreads();
                 if (tid == 0) {
                     fence_acq_rel();  // publishes Rp
@@ -706,7 +787,9 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
             }
         } else {
             if (tid == 0)
-                s_ok = wait_at_least(col_done + task.b, (unsigned)(planes_in(p, task.b) * S::CT), err);
+                s_ok = wait_at_least(col_done + task.b,
+                                     p.stall ? 0xffffffffu : (unsigned)(planes_in(p, task.b) * S::CT),
+                                     err, p.wait_limit);
             __syncthreads();
             if (s_ok) {
                 row_task<N, OBJ, SSB1>(p, smem, task.b, task.idx, planes_in(p, task.b), plane_free,
@@ -727,7 +810,8 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
 
 // ---------------------------------------------------------------- loss
 
-// L = (1/P) sum_r [S2(r)/n - (S1(r)/n)^2], with S2 summed per row task.  Each block reduces
+// L = (1/P) sum_r [S2(r)/n - (S1(r)/n)^2], with S2 summed per row task (NaN when the
+// error word is raised).  Each block reduces
 // one contiguous range of pixels in a fixed order (strided per thread, then a shared-memory
 // tree) into part[block]; the block that finishes last (counted in *cnt, cleared with the
 // scheduler words before every evaluation) adds the partials in block order and the row
@@ -737,7 +821,8 @@ constexpr int kLossBlocks = 128, kLossThreads = 256;
 __global__ void __launch_bounds__(kLossThreads) k_loss_fused(const double *__restrict__ S1,
                                                              const double *__restrict__ S2g, int nr,
                                                              int P, double inv_n, double *part,
-                                                             unsigned *cnt, double *__restrict__ out) {
+                                                             unsigned *cnt, const unsigned *err,
+                                                             double *__restrict__ out) {
     __shared__ double red[kLossThreads];
     __shared__ unsigned s_rank;
     const int tid = threadIdx.x;
@@ -745,7 +830,7 @@ __global__ void __launch_bounds__(kLossThreads) k_loss_fused(const double *__res
     const int i0 = blockIdx.x * per, i1 = min(P, i0 + per);
     double acc = 0.0;
     for (int i = i0 + tid; i < i1; i += kLossThreads) {
-        const double m = S1[i] * inv_n;
+        const double m = s1_value(S1, i) * inv_n;
         acc -= m * m;
     }
     red[tid] = acc;
@@ -765,7 +850,8 @@ __global__ void __launch_bounds__(kLossThreads) k_loss_fused(const double *__res
     double sm = 0.0, s2 = 0.0;
     for (int b = 0; b < kLossBlocks; ++b) sm += __ldcg(part + b);
     for (int r = 0; r < nr; ++r) s2 += S2g[r] * inv_n;
-    *out = (s2 + sm) / (double)P;
+    // a wait of this library call gave up (here or in an earlier trial): no valid loss
+    *out = *err != 0u ? __longlong_as_double(0x7ff8000000000000LL) : (s2 + sm) / (double)P;
 }
 
 // ---------------------------------------------------------------- host side
@@ -775,7 +861,7 @@ static int row_tasks_for(int N) {
     return N / std::min(groups, N);
 }
 
-// scheduler words, then the loss kernel's block counter (the last word)
+// error word, scheduler words, then the loss kernel's block counter (the last word)
 size_t fused_sync_words(int N, int n_bf, int Bk) {
     const int nbatch = (n_bf + Bk - 1) / Bk;
     return 2 + (size_t)nbatch * (1 + 2 * (size_t)Bk) + (size_t)row_tasks_for(N) + 1;
@@ -864,8 +950,10 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     if ((e = cudaMemsetAsync(a.S2g, 0, sizeof(double) * S::NR, s)) != cudaSuccess) return e;
     if (want_object && (e = cudaMemsetAsync(a.Osum, 0, sizeof(double2) * P, s)) != cudaSuccess)
         return e;
-    if ((e = cudaMemsetAsync(a.sync, 0, sizeof(unsigned) * fused_sync_words(N, a.n_bf, a.Bk), s)) !=
-        cudaSuccess)
+    // every scheduler word but the error word (word 0), which the caller clears once per
+    // library call so that a wait that ran out in any trial of a batch is still reported
+    if ((e = cudaMemsetAsync(a.sync + 1, 0, sizeof(unsigned) * (fused_sync_words(N, a.n_bf, a.Bk) - 1),
+                             s)) != cudaSuccess)
         return e;
     FusedParams fp;
     fp.G = a.G;
@@ -884,13 +972,15 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     fp.Bk = a.Bk;
     fp.nbatch = nbatch;
     fp.D = a.D;
+    fp.wait_limit = a.wait_limit ? a.wait_limit : kWaitLimit;
+    fp.stall = a.stall;
     fp.tc = make_trial_const(a, th, N);
     e = want_object ? fused_launch<N, true, SSB1>(fp, s) : fused_launch<N, false, SSB1>(fp, s);
     if (e != cudaSuccess) return e;
     prof_begin("k_loss", s);
     k_loss_fused<<<kLossBlocks, kLossThreads, 0, s>>>(
         a.S1, a.S2g, S::NR, (int)P, 1.0 / a.n_bf, a.S2g + S::NR,
-        a.sync + fused_sync_words(N, a.n_bf, a.Bk) - 1, loss_slot);
+        a.sync + fused_sync_words(N, a.n_bf, a.Bk) - 1, a.sync, loss_slot);
     prof_end(s);
     count_launch();
     return cudaGetLastError();

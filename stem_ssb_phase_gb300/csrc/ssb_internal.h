@@ -60,6 +60,8 @@ struct ObjectiveArgs {
     int D;                  // ring slots
     int mode;               // 0 SSB2, 1 SSB1
     double step, lam, semi, dalpha;  // geometry (Angstrom, rad)
+    unsigned wait_limit;    // polls before a scheduler wait gives up (0: the default)
+    int stall;              // test hook: row tasks wait for a count never reached
 };
 
 TrialHost trial_host(const ssb_params &t);
@@ -76,7 +78,10 @@ size_t fused_rring_elems(int N, int Bk, int D);
 int fused_row_tasks(int N);
 size_t fused_s2g_elems(int N);  // per row task S2 sums, then the loss kernel's block partials
 // One full objective evaluation on the persistent fused kernel (accumulators and
-// scheduler words cleared first), loss written to *loss_slot.
+// scheduler words cleared first), loss written to *loss_slot.  The error word (sync[0]) is
+// not cleared here: the caller clears it once per library call and reads it at the end, so
+// a wait that ran out in any evaluation of the call is reported (and every later loss of
+// the call is NaN).
 cudaError_t run_objective_fused(const ObjectiveArgs &a, const ssb_params &theta, double *loss_slot,
                                 bool want_object, cudaStream_t s);
 

@@ -1,15 +1,19 @@
 // ssb_loss_noalloc: the SSB2 objective for callers that must not allocate device memory.
 //
-// Some callers cannot call cudaMalloc at the point where they need a loss: code that runs
-// while one of its streams is being captured into a CUDA graph (device allocation is not
-// allowed in capture), real-time pipelines that plan all memory up front and forbid
-// allocation afterwards, and plug-ins that live inside a host application which owns the
-// GPU memory through its own allocator.  This entry point serves them: every byte of
+// Some callers cannot call cudaMalloc at the point where they need a loss: real-time
+// pipelines that plan all device memory up front and forbid allocation afterwards (an
+// allocation can block on the driver and break their timing), and plug-ins that live
+// inside a host application which owns the GPU memory through its own allocator (memory
+// taken behind its back can make the host's own allocations fail).  This entry point
+// serves them: every byte of
 // scratch it needs (per-trial tables, per-BF geometry, the column-to-row ring, the
 // accumulators and the scheduler words) lives in one file-scope device array of fixed
 // size, reserved when the library's device code is loaded on a GPU and kept until the
 // process exits.  It runs the same persistent kernel as ssb_loss_batch, with a smaller
 // batch and ring so that the whole scratch stays modest.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstring>
 #include <mutex>
 
@@ -27,21 +31,51 @@ constexpr int kMaxDevices = 64;
 // address: host code obtains the address with cudaGetSymbolAddress (below).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
+// Per device: the scratch's device address and the id of the context it was looked up in.
 static void *g_scratch_addr[kMaxDevices];
+static unsigned long long g_scratch_ctx[kMaxDevices];
 static std::mutex g_scratch_mu;
 
-// Device address of the scratch on the current device, looked up once per device.
+// Unique id of the current context (0 if the driver cannot say); a device whose context was
+// destroyed (cudaDeviceReset) and created again gets a new id, and its module a new address.
+static unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
+
+// Device address of the scratch on the current device.  Set-up: looked up with
+// cudaGetSymbolAddress on the first call on each device (with that device current), and
+// again whenever the device's context has changed since (after cudaDeviceReset).
 static cudaError_t scratch_base(unsigned char **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const unsigned long long ctx = current_context_id();  // 0 before the context exists
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // creates the context if needed
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx ? ctx : current_context_id();
     }
     *out = (unsigned char *)g_scratch_addr[dev];
     return cudaSuccess;
@@ -161,10 +195,11 @@ extern "C" ssb_status ssb_loss_noalloc(const ssb_geometry *g, const void *g_cach
     a.semi = g->semiangle_mrad * 1e-3;
     a.dalpha = g->det_sampling_mrad * 1e-3;
 
-    // per-BF geometry and twiddles into the scratch (the accumulators and scheduler words
-    // are cleared by the objective itself before its kernel runs)
+    // per-BF geometry and twiddles into the scratch, and the error word cleared (the
+    // accumulators and the other scheduler words are cleared by the objective itself)
     e = cudaMemcpyAsync(base + L.yx, g->bf_det_yx, sizeof(float) * 2 * (size_t)g->n_bf,
                         cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.sync, 0, sizeof(unsigned), s);
     if (e == cudaSuccess) {
         k_noalloc_geometry<<<(g->n_bf + 127) / 128, 128, 0, s>>>(
             (const float *)(base + L.yx), g->n_bf, a.dalpha, a.semi, (float4 *)(base + L.kgeo),
@@ -175,16 +210,19 @@ extern "C" ssb_status ssb_loss_noalloc(const ssb_geometry *g, const void *g_cach
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = run_objective_fused(a, *theta, a.loss, false, s);
+    // the loss and the error word land in host locals; *loss_out is written only on success
     unsigned err_word = 0;
+    double loss = 0.0;
     if (e == cudaSuccess)
-        e = cudaMemcpyAsync(loss_out, a.loss, sizeof(double), cudaMemcpyDeviceToHost, s);
+        e = cudaMemcpyAsync(&loss, a.loss, sizeof(double), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess)
-        e = cudaMemcpyAsync(&err_word, a.sync + 1, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
+        e = cudaMemcpyAsync(&err_word, a.sync, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return fail(SSB_ERR_CUDA, cudaGetErrorString(e));
     }
     if (err_word) return fail(SSB_ERR_TIMEOUT, "a scheduler wait in the fused objective kernel ran out");
+    *loss_out = loss;
     return SSB_OK;
 }

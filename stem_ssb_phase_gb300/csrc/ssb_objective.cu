@@ -56,7 +56,7 @@ __global__ void k_finalize(const double *__restrict__ S1, const double2 *__restr
                            float2 *__restrict__ obj) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= P) return;
-    mean_phase[i] = (float)(S1[i] * inv_n);
+    mean_phase[i] = (float)(s1_value(S1, i) * inv_n);
     if (obj) {
         const double2 o = Osum[i];
         obj[i] = make_float2((float)(o.x * obj_scale), (float)(o.y * obj_scale));

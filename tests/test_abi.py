@@ -10,7 +10,9 @@ import pytest
 import stem_ssb_phase_gb300 as ssbgpu
 from stem_ssb_phase_gb300 import build as ssbbuild
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "ssb.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
+HEADER = os.path.join(INCLUDE, "ssb.h")
+DEBUG_HEADER = os.path.join(INCLUDE, "ssb_debug.h")
 
 
 @pytest.fixture(scope="module")
@@ -19,20 +21,33 @@ def lib():
     return ssbgpu.load_library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(path=HEADER):
+    text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(ssb_[a-z_0-9]+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_exports():
     assert set(declared_functions()) == set(ssbgpu.EXPORTS)
+    assert set(declared_functions(DEBUG_HEADER)) == set(ssbgpu.DEBUG_EXPORTS)
 
 
-def test_every_declared_symbol_is_exported(lib):
-    for name in declared_functions():
+def test_every_header_is_covered():
+    assert sorted(os.listdir(INCLUDE)) == ["ssb.h", "ssb_debug.h"]
+
+
+@pytest.mark.parametrize("header", [HEADER, DEBUG_HEADER])
+def test_every_declared_symbol_is_exported(lib, header):
+    for name in declared_functions(header):
         assert hasattr(lib, name), name
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_test_hooks_reject_bad_arguments_on_the_host(lib):
+    assert lib.ssb_debug_stall_next(None, 0, 4) == 1
+    assert lib.ssb_debug_poison_scratch(None, None) == 1
+    assert lib.ssb_debug_atan2(None, None, 4, None, None) == 1
+    assert lib.ssb_debug_atan2(None, None, 0, None, None) == 0  # n = 0 is a no-op
 
 
 def test_status_strings(lib):
