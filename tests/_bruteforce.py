@@ -2,11 +2,16 @@
 
 Written independently of the vectorised oracle: direct double sums for both
 transforms on the full grid (no half-plane, no mirror rule, no FFT), per-point
-transfer evaluation with cmath, and explicit moment loops.  Only usable for N <= 8
-and a handful of BF pixels.
+transfer evaluation with cmath, and explicit moment loops.  The aperture amplitudes come
+from 50-digit arithmetic on the exact input values, so an amplitude is zero only when it
+is zero exactly (the oracle reaches the same zeros through its 2^-16 floor; where the two
+could differ, genuine amplitudes below 2^-16, the floor's own pins count them).  Only
+usable for N <= 8 and a handful of BF pixels.
 """
 import cmath
 import math
+
+import mpmath
 
 
 def _signed(q, n):
@@ -14,10 +19,19 @@ def _signed(q, n):
     return q if q < n // 2 else q - n
 
 
-def _probe(ax, ay, lam, semi, da, c10, c12, phi12):
-    amp = min(1.0, max(0.0, (semi - math.hypot(ax, ay)) / da + 0.5))
-    if amp < 2.0 ** -16:  # zero-transfer floor of the aperture
-        amp = 0.0
+def _amplitude(ax, ay, semi, da):
+    """Soft aperture clip((semi - |alpha|)/da + 1/2, 0, 1) evaluated in 50-digit arithmetic
+    from the arguments' exact values (mpmath numbers or floats), so that zero means exactly
+    zero: no floor, no float64 rounding at the edge."""
+    with mpmath.workdps(50):
+        a = (mpmath.mpf(semi) - mpmath.sqrt(ax * ax + ay * ay)) / mpmath.mpf(da) + mpmath.mpf(1) / 2
+        return float(min(max(a, 0), 1))
+
+
+def _probe(ax, ay, lam, semi, da, c10, c12, phi12, amp=None):
+    if amp is None:
+        amp = _amplitude(ax, ay, semi, da)
+    ax, ay = float(ax), float(ay)
     ph = (math.pi / lam) * (c10 * (ax * ax + ay * ay)
                             + c12 * ((ax * ax - ay * ay) * math.cos(2 * phi12)
                                      + 2 * ax * ay * math.sin(2 * phi12)))
@@ -32,6 +46,8 @@ def objective_loops(counts, geom, theta, mode="ssb2"):
     da = geom.det_sampling_mrad * 1e-3
     c10, c12, phi12, rot = theta[0] * 10.0, theta[1] * 10.0, theta[2], theta[3]
     cr, sr = math.cos(rot), math.sin(rot)
+    with mpmath.workdps(50):
+        mcr, msr = mpmath.cos(mpmath.mpf(rot)), mpmath.sin(mpmath.mpf(rot))
     nb = len(geom.bf_det_yx)
     s1 = [[0.0] * n for _ in range(n)]
     s2 = [[0.0] * n for _ in range(n)]
@@ -39,6 +55,9 @@ def objective_loops(counts, geom, theta, mode="ssb2"):
     for k in range(nb):
         ay_k = float(geom.bf_det_yx[k][0]) * da
         ax_k = float(geom.bf_det_yx[k][1]) * da
+        with mpmath.workdps(50):
+            may_k = mpmath.mpf(float(geom.bf_det_yx[k][0])) * mpmath.mpf(da)
+            max_k = mpmath.mpf(float(geom.bf_det_yx[k][1])) * mpmath.mpf(da)
         img = [[float(counts[k][y][x]) for x in range(n)] for y in range(n)]
         # forward DFT on the full grid
         spec = [[0j] * n for _ in range(n)]
@@ -61,8 +80,16 @@ def objective_loops(counts, geom, theta, mode="ssb2"):
                 fy = _signed(qy, n) / (n * geom.scan_step_A)
                 lx = lam * (cr * fx - sr * fy)
                 ly = lam * (sr * fx + cr * fy)
-                am, pm = _probe(ax_k - lx, ay_k - ly, lam, semi, da, c10, c12, phi12)
-                ap, pp = _probe(ax_k + lx, ay_k + ly, lam, semi, da, c10, c12, phi12)
+                # the shifted apertures' amplitudes from the exact shifted arguments
+                with mpmath.workdps(50):
+                    mfx = mpmath.mpf(_signed(qx, n)) / (n * mpmath.mpf(geom.scan_step_A))
+                    mfy = mpmath.mpf(_signed(qy, n)) / (n * mpmath.mpf(geom.scan_step_A))
+                    mlx = mpmath.mpf(lam) * (mcr * mfx - msr * mfy)
+                    mly = mpmath.mpf(lam) * (msr * mfx + mcr * mfy)
+                    amp_m = _amplitude(max_k - mlx, may_k - mly, semi, da)
+                    amp_p = _amplitude(max_k + mlx, may_k + mly, semi, da)
+                am, pm = _probe(ax_k - lx, ay_k - ly, lam, semi, da, c10, c12, phi12, amp_m)
+                ap, pp = _probe(ax_k + lx, ay_k + ly, lam, semi, da, c10, c12, phi12, amp_p)
                 if mode == "ssb2":
                     term1 = ak_amp * am * cmath.exp(1j * (pm - ak_ph))
                     term2 = ak_amp * ap * cmath.exp(1j * (ak_ph - pp))
