@@ -95,9 +95,14 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
 /* Exact objective for T trials (page "SSB performance notes", multi-candidate
  * evaluation: each trial keeps its own correction, FFTs, phase and loss).  Here each
  * trial is one launch of the persistent kernel, which reads the G cache once; the G read
- * is not what bounds the kernel, so trials do not share it.  theta: host [T]; loss_out:
- * host [T] (float64).  T >= 1.  Each entry equals the loss of a single-trial call with the
- * same theta, bit for bit; the transfer is the context's. */
+ * is not what bounds the kernel, so trials do not share it.  Consecutive trials alternate
+ * between cuda_stream and a second stream of the context (each with its own buffers), so
+ * that one launch's last tasks overlap the next launch's start; the call is still ordered
+ * after earlier work on cuda_stream, and later work on cuda_stream after it.  theta: host
+ * [T]; loss_out: host [T] (float64).  T >= 1.  Each entry equals the loss of a
+ * single-trial call with the same theta, bit for bit; the transfer is the context's.
+ * SSB_ERR_TIMEOUT: a bounded wait of the kernel ran out; the losses of that trial and of
+ * every later one are NaN, and so may be the loss of the trial that overlapped it. */
 ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *loss_out,
                           void *cuda_stream);
 

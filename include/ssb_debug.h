@@ -20,7 +20,8 @@ extern "C" {
  * wait for a completion count that nothing ever reaches, with a poll limit of `polls`
  * (0 is taken as 1).  The wait then gives up, raises the kernel's error word, every other
  * wait stops, the kernel returns, and the call reports SSB_ERR_TIMEOUT; the losses of that
- * trial and of every later trial of the call are NaN.  The hook is consumed by that call.
+ * trial and of every later trial of the call are NaN (and so may be the loss of the trial
+ * before it, whose launch overlaps it on the GPU).  The hook is consumed by that call.
  * This is the timeout behaviour of the boundary (status codes only, no trap); the pages
  * define no counterpart.  NULL c or evaluation < 0 -> SSB_ERR_ARG. */
 ssb_status ssb_debug_stall_next(ssb_ctx *c, int evaluation, unsigned polls);

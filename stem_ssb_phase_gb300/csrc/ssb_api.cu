@@ -92,6 +92,18 @@ struct DeviceGuard {
 
 using namespace ssb;
 
+// The buffers one evaluation in flight works in: per-trial tables, the column-to-row ring,
+// the accumulators and the scheduler words.  A context holds two sets, so that consecutive
+// trials of a batch can overlap on the GPU.
+struct TrialSet {
+    uint2 *kturn = nullptr;
+    float2 *E = nullptr;
+    double *S1 = nullptr;
+    float2 *Zring = nullptr, *hring = nullptr, *rring = nullptr;
+    double *S2g = nullptr;
+    unsigned *sync = nullptr;
+};
+
 struct ssb_ctx {
     int dev = 0;
     int N = 0, n_bf = 0;
@@ -100,17 +112,16 @@ struct ssb_ctx {
     float2 *G = nullptr;
     float4 *kgeo = nullptr;
     double2 *kalpha = nullptr;
-    uint2 *kturn = nullptr;
-    float2 *E = nullptr;
     float2 *tw = nullptr;
-    double *S1 = nullptr;
-    double2 *Osum = nullptr;
+    TrialSet set[2];
+    double2 *Osum = nullptr;  // object sums (set 0 only: ssb_reconstruct)
     double *loss = nullptr;
     int loss_cap = 0;
-    float2 *Zring = nullptr, *hring = nullptr, *rring = nullptr;
-    double *S2g = nullptr;
-    unsigned *sync = nullptr;
+    unsigned *err = nullptr;  // error word of the current library call
     int Bk = 0, D = 0;
+    // second stream of a batch (odd trials) and the events that fork and join it
+    cudaStream_t aux = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     int *flag = nullptr;
     size_t g_bytes = 0, scratch_bytes = 0;
     // upsampled redraw scratch, allocated on first use for the largest factor seen
@@ -124,24 +135,26 @@ struct ssb_ctx {
     int dbg_stall_eval = -1;
     unsigned dbg_wait_limit = 0;
 
-    ObjectiveArgs args() const {
+    ObjectiveArgs args(int si = 0) const {
+        const TrialSet &t = set[si];
         ObjectiveArgs a;
         a.N = N;
         a.n_bf = n_bf;
         a.G = G;
         a.kgeo = kgeo;
         a.kalpha = kalpha;
-        a.kturn = kturn;
-        a.E = E;
+        a.kturn = t.kturn;
+        a.E = t.E;
         a.tw = tw;
-        a.S1 = S1;
-        a.Osum = Osum;
+        a.S1 = t.S1;
+        a.Osum = si == 0 ? Osum : nullptr;
         a.loss = loss;
-        a.Zring = Zring;
-        a.hring = hring;
-        a.rring = rring;
-        a.S2g = S2g;
-        a.sync = sync;
+        a.Zring = t.Zring;
+        a.hring = t.hring;
+        a.rring = t.rring;
+        a.S2g = t.S2g;
+        a.sync = t.sync;
+        a.err = err;
         a.Bk = Bk;
         a.D = D;
         a.mode = transfer == SSB_TRANSFER_SSB1 ? 1 : 0;
@@ -157,20 +170,28 @@ struct ssb_ctx {
 
 static void free_ctx(ssb_ctx *c) {
     if (!c) return;
-    void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->kturn, c->E, c->tw, c->S1, c->Osum,
-                    c->loss, c->flag, c->Zring, c->hring, c->rring, c->S2g, c->sync,
+    void *ptrs[] = {c->G, c->kgeo, c->kalpha, c->tw, c->Osum, c->loss, c->err, c->flag,
                     c->up_T,  c->up_tab, c->rd_part, c->rd_S, c->rd_T};
     for (void *p : ptrs)
         if (p) cudaFree(p);
+    for (const TrialSet &t : c->set) {
+        void *tp[] = {t.kturn, t.E, t.S1, t.Zring, t.hring, t.rring, t.S2g, t.sync};
+        for (void *p : tp)
+            if (p) cudaFree(p);
+    }
+    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+    if (c->ev_join) cudaEventDestroy(c->ev_join);
+    if (c->aux) cudaStreamDestroy(c->aux);
     delete c;
 }
 
 static bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
 
-// Evaluation number `index` of the current library call (the stall test hook applies to one).
+// Evaluation number `index` of the current library call (the stall test hook applies to
+// one), in buffer set `si`.
 static cudaError_t evaluate(const ssb_ctx *c, const ssb_params &theta, double *loss_slot,
-                            bool want_object, cudaStream_t s, int index = 0) {
-    ObjectiveArgs a = c->args();
+                            bool want_object, cudaStream_t s, int index = 0, int si = 0) {
+    ObjectiveArgs a = c->args(si);
     if (index == c->dbg_stall_eval) {
         a.stall = 1;
         a.wait_limit = c->dbg_wait_limit;
@@ -181,7 +202,7 @@ static cudaError_t evaluate(const ssb_ctx *c, const ssb_params &theta, double *l
 // Start of a library call that evaluates the objective: clear the scheduler's error word
 // (it stays raised for the rest of the call once a wait has run out).
 static ssb_status begin_call(const ssb_ctx *c, cudaStream_t s) {
-    SSB_CK(cudaMemsetAsync(c->sync, 0, sizeof(unsigned), s));
+    SSB_CK(cudaMemsetAsync(c->err, 0, sizeof(unsigned), s));
     return SSB_OK;
 }
 
@@ -191,7 +212,7 @@ static ssb_status check_sync(ssb_ctx *c, cudaStream_t s) {
     c->dbg_stall_eval = -1;
     c->dbg_wait_limit = 0;
     unsigned h = 0;
-    SSB_CK(cudaMemcpyAsync(&h, c->sync, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+    SSB_CK(cudaMemcpyAsync(&h, c->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
     SSB_CK(cudaStreamSynchronize(s));
     if (h) return fail(SSB_ERR_TIMEOUT, "a scheduler wait in the fused objective kernel ran out");
     return SSB_OK;
@@ -292,8 +313,6 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     SSB_ALLOC(c->G, (size_t)c->n_bf * H * N, gb);
     SSB_ALLOC(c->kgeo, (size_t)c->n_bf, sb);
     SSB_ALLOC(c->kalpha, (size_t)c->n_bf, sb);
-    SSB_ALLOC(c->kturn, (size_t)c->n_bf, sb);
-    SSB_ALLOC(c->E, P, sb);
     SSB_ALLOC(c->tw, (size_t)N, sb);
     // Both transfers run on the persistent fused kernel.  Batch size and ring depth: four
     // batches in flight keep the column work flowing while row tasks drain the oldest
@@ -304,18 +323,29 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     const bool ssb1 = transfer == SSB_TRANSFER_SSB1;
     c->Bk = std::min(ssb1 ? SSB_FUSED_BK / 2 : SSB_FUSED_BK, c->n_bf);
     c->D = SSB_FUSED_RING;
-    SSB_ALLOC(c->Zring, fused_ring_elems(N, c->Bk, c->D, ssb1), sb);
-    SSB_ALLOC(c->hring, fused_hring_elems(N, c->Bk, c->D), sb);
-    SSB_ALLOC(c->rring, fused_rring_elems(N, c->Bk, c->D), sb);
-    SSB_ALLOC(c->S2g, fused_s2g_elems(N), sb);
-    SSB_ALLOC(c->sync, fused_sync_words(N, c->n_bf, c->Bk), sb);
-    SSB_ALLOC(c->S1, P, sb);
+    for (TrialSet &t : c->set) {
+        SSB_ALLOC(t.kturn, (size_t)c->n_bf, sb);
+        SSB_ALLOC(t.E, P, sb);
+        SSB_ALLOC(t.Zring, fused_ring_elems(N, c->Bk, c->D, ssb1), sb);
+        SSB_ALLOC(t.hring, fused_hring_elems(N, c->Bk, c->D), sb);
+        SSB_ALLOC(t.rring, fused_rring_elems(N, c->Bk, c->D), sb);
+        SSB_ALLOC(t.S2g, fused_s2g_elems(N), sb);
+        SSB_ALLOC(t.sync, fused_sync_words(N, c->n_bf, c->Bk), sb);
+        SSB_ALLOC(t.S1, P, sb);
+    }
     SSB_ALLOC(c->Osum, P, sb);
+    SSB_ALLOC(c->err, (size_t)1, sb);
     c->loss_cap = 4096;
     SSB_ALLOC(c->loss, (size_t)c->loss_cap, sb);
     SSB_ALLOC(c->flag, (size_t)1, sb);
     c->g_bytes = gb;
     c->scratch_bytes = sb;
+    if ((e = cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming)) != cudaSuccess) {
+        st = cuda_fail(e, "stream or event creation");
+        return bail(st);
+    }
 
     // per-BF geometry (float64 on the host)
     std::vector<float4> kgeo(c->n_bf);
@@ -410,11 +440,25 @@ ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *lo
     cudaStream_t s = (cudaStream_t)cuda_stream;
     ssb_status st = begin_call(c, s);
     if (st != SSB_OK) return st;
+    // Consecutive trials alternate between the caller's stream (buffer set 0) and the
+    // context's second stream (set 1), so that the end of one persistent launch, where its
+    // last row tasks leave most SMs idle, overlaps the per-trial tables and the first
+    // column tasks of the next.  Each trial's arithmetic is the same as a scalar call's.
     for (int t0 = 0; t0 < T; t0 += c->loss_cap) {
         const int tn = std::min(c->loss_cap, T - t0);
+        const bool overlap = tn >= 2;
+        if (overlap) {
+            SSB_CK(cudaEventRecord(c->ev_fork, s));
+            SSB_CK(cudaStreamWaitEvent(c->aux, c->ev_fork, 0));
+        }
         for (int t = 0; t < tn; ++t) {
-            cudaError_t e = evaluate(c, theta[t0 + t], c->loss + t, false, s, t0 + t);
+            const int si = overlap ? (t & 1) : 0;
+            cudaError_t e = evaluate(c, theta[t0 + t], c->loss + t, false, si ? c->aux : s, t0 + t, si);
             if (e != cudaSuccess) return cuda_fail(e, "objective launch");
+        }
+        if (overlap) {
+            SSB_CK(cudaEventRecord(c->ev_join, c->aux));
+            SSB_CK(cudaStreamWaitEvent(s, c->ev_join, 0));
         }
         SSB_CK(cudaMemcpyAsync(loss_out + t0, c->loss, sizeof(double) * tn, cudaMemcpyDeviceToHost, s));
         // the error word is cleared once per call, so this sees a wait that ran out in any
@@ -682,18 +726,22 @@ ssb_status ssb_debug_poison_scratch(ssb_ctx *c, void *cuda_stream) {
     struct Buf {
         void *p;
         size_t bytes;
-    } bufs[] = {
-        {c->Zring, fused_ring_elems(c->N, c->Bk, c->D, ssb1) * sizeof(float2)},
-        {c->hring, fused_hring_elems(c->N, c->Bk, c->D) * sizeof(float2)},
-        {c->rring, fused_rring_elems(c->N, c->Bk, c->D) * sizeof(float2)},
-        {c->S2g, fused_s2g_elems(c->N) * sizeof(double)},
-        {c->sync, fused_sync_words(c->N, c->n_bf, c->Bk) * sizeof(unsigned)},
-        {c->S1, P * sizeof(double)},
-        {c->Osum, P * sizeof(double2)},
-        {c->E, P * sizeof(float2)},
-        {c->kturn, (size_t)c->n_bf * sizeof(uint2)},
-        {c->loss, (size_t)c->loss_cap * sizeof(double)},
     };
+    std::vector<Buf> bufs = {
+        {c->Osum, P * sizeof(double2)},
+        {c->loss, (size_t)c->loss_cap * sizeof(double)},
+        {c->err, sizeof(unsigned)},
+    };
+    for (const TrialSet &t : c->set) {
+        bufs.push_back({t.Zring, fused_ring_elems(c->N, c->Bk, c->D, ssb1) * sizeof(float2)});
+        bufs.push_back({t.hring, fused_hring_elems(c->N, c->Bk, c->D) * sizeof(float2)});
+        bufs.push_back({t.rring, fused_rring_elems(c->N, c->Bk, c->D) * sizeof(float2)});
+        bufs.push_back({t.S2g, fused_s2g_elems(c->N) * sizeof(double)});
+        bufs.push_back({t.sync, fused_sync_words(c->N, c->n_bf, c->Bk) * sizeof(unsigned)});
+        bufs.push_back({t.S1, P * sizeof(double)});
+        bufs.push_back({t.E, P * sizeof(float2)});
+        bufs.push_back({t.kturn, (size_t)c->n_bf * sizeof(uint2)});
+    }
     for (const Buf &b : bufs) SSB_CK(cudaMemsetAsync(b.p, 0xff, b.bytes, s));
     SSB_CK(cudaStreamSynchronize(s));
     return SSB_OK;

@@ -25,7 +25,8 @@
 //       task that completes a plane's column pass also transforms its Nyquist-row term;
 //   row task (batch b, RT rows): for each plane of the batch, rebuild the full rows (SSB2)
 //       or take them as they are (SSB1), row IFFT, phi = atan2, accumulate; then add the
-//       batch's per-pixel sums into the float64 S1 (and S2, object) in batch order.
+//       batch's per-pixel sums into S1 (a float pair per pixel, exact two-sum; S2 and the
+//       object in float64) in batch order.
 // A block takes its next ticket when its current task has finished its work: a column
 // task just before its completion fence (the round trips overlap), a row task after its
 // signal.  (Taking a column ticket any earlier, even just before the task's ring writes,
@@ -67,11 +68,13 @@ struct FusedParams {
     float2 *Z;            // ring [D][Bk][H][N]: column-pass output, one column contiguous
     float2 *hrow;         // ring [D][Bk][LDZ], Nyquist-row Hermitian parts
     float2 *rrow;         // ring [D][Bk][N/2]: Rp(2j) + i Rp(2j+1), Rp the Nyquist-row term
-    double *S1;           // [P]
+    double *S1;           // [P] 8 bytes per pixel, stored as float2 (hi, lo): see df_add
     double *S2g;          // [row tasks]
     double2 *Osum;        // [P] (object redraw only)
-    unsigned *sync;       // error, ticket, col_done[nbatch], plane_free[nbatch][Bk],
+    unsigned *sync;       // ticket, col_done[nbatch], plane_free[nbatch][Bk],
                           // h_cnt[nbatch][Bk], chain[row tasks]
+    unsigned *err;        // error word, cleared once per library call (shared by the
+                          // evaluations of a call, so a timeout stays raised)
     int n_bf, Bk, nbatch;
     int D;                // ring slots (batches in flight)
     unsigned wait_limit;  // polls before a wait gives up (kWaitLimit unless a test lowers it)
@@ -89,13 +92,12 @@ struct FusedShape {
     static constexpr int H = SSB1 ? N : N / 2 + 1;  // columns corrected and column-transformed
     static constexpr int M = SSB1 ? N : N / 2;      // row transform length
     static constexpr int RE = SSB1 ? kPts : 8;      // row transform points per thread (M / T)
-    // Column tasks cover HC columns per plane; the SSB2 column N/2 is transformed by the
-    // task that completes the plane (beside the Nyquist-row term), so that for N = 512 the
-    // 256 task columns split evenly into tasks.
-    static constexpr int HC = SSB1 ? N : N / 2;
     static constexpr int CW = GROUPS * kColsPerWarp;  // columns per column task
     static constexpr int RT = GROUPS < N ? GROUPS : N;  // rows per row task (multiple of 4)
-    static constexpr int CT = (HC + CW - 1) / CW;   // column tasks per plane
+    // Column tasks per plane.  (For SSB2 at N = 512 the last of the 17 takes column N/2
+    // alone; moving that column into the task that completes the plane, beside the
+    // Nyquist-row term, measured slower: it lengthens each plane's critical path.)
+    static constexpr int CT = (H + CW - 1) / CW;
     static constexpr int NR = N / RT;               // row tasks per trial
     static constexpr int SMF = RegFFT<N, kPts>::SMEM;  // FFT scratch per group
     static constexpr int LDZ = (N / 2 + 1 + 7) / 8 * 8;  // h row stride (64 B multiple)
@@ -345,8 +347,7 @@ __device__ __forceinline__ void column_store(const FusedParams &p, int slot, int
     if (hstore) __stcg(p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ + nx, hval);
 }
 
-// One column task: CW of the plane's HC task columns (SSB2: 0 .. N/2 - 1, the task that
-// completes the plane then adds column N/2; SSB1: all N), kColsPerWarp per transform
+// One column task: CW of the plane's H transformed columns, kColsPerWarp per transform
 // group in turn.  free_word (NULL on the slot's first use) counts the row tasks of batch
 // b - D that have released this plane of the ring slot; the task overwrites the plane only
 // once all of them have.  Each warp reads the count when the task starts and checks it
@@ -368,7 +369,7 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
 #pragma unroll 1
     for (int c = 0; c < kColsPerWarp; ++c) {
         const int nx = ct * S::CW + c * S::GROUPS + grp;
-        const bool valid = nx < S::HC;
+        const bool valid = nx < S::H;
         float2 v[kPts];
         float2 hval;
         bool hstore;
@@ -382,23 +383,6 @@ __device__ int column_task(const FusedParams &p, float2 *smem, int b, int idx,
         if (valid && ok) column_store<N, SSB1>(p, slot, kk, nx, v, hval, hstore);
     }
     return ok;
-}
-
-// The SSB2 column N/2 of plane kk (ring slot `slot`) of batch b, by one warp (its first
-// transform group stores), in the task that completes the plane's column pass.  The warp
-// already waited for the plane to be free in that task (ok).
-template <int N>
-__device__ void half_column(const FusedParams &p, float2 *smem, int b, int kk) {
-    using S = FusedShape<N, false>;
-    const int k = b * p.Bk + kk;
-    const float4 geo = __ldg(p.kgeo + k);
-    const uint2 bt = __ldg(p.kturn + k);
-    const bool first = (threadIdx.x & 31) < S::T;  // the warp's first group
-    float2 v[kPts];
-    float2 hval;
-    bool hstore;
-    column_compute<N, false>(p, smem, k, N / 2, first, geo, bt, v, hval, hstore);
-    if (first) column_store<N, false>(p, b % p.D, kk, N / 2, v, hval, false);
 }
 
 // ---------------------------------------------------------------- row task
@@ -571,7 +555,8 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             }
         }
     }
-    // Add this batch into the float64 accumulators.  Only this update is ordered: it
+    // Add this batch into the accumulators (S1 by exact two-sums into its float pair, the
+    // object sums in float64).  Only this update is ordered: it
     // waits until the previous batch's task for the same rows has made its own update,
     // which keeps the per-pixel summation order fixed while the tasks themselves overlap.
     if (tid == 0) *s_ok = wait_at_least(chain + rt, (unsigned)b, err, p.wait_limit);
@@ -580,7 +565,6 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         // pixel j + T r of row ry holds acc1[r]; loads are issued in groups ahead of their
         // stores (a store through the same pointer would hold back each following load)
         constexpr int GS = OBJ ? 4 : 16;
-#if SSB_S1_DF
         float2 *s1 = reinterpret_cast<float2 *>(p.S1 + (size_t)ry * N) + j;
 #pragma unroll
         for (int g0 = 0; g0 < 16; g0 += GS) {
@@ -590,17 +574,6 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
 #pragma unroll
             for (int r = 0; r < GS; ++r) s1[S::T * (g0 + r)] = df_add(old[r], acc1[g0 + r]);
         }
-#else
-        double *s1 = p.S1 + (size_t)ry * N + j;
-#pragma unroll
-        for (int g0 = 0; g0 < 16; g0 += GS) {
-            double old[GS];
-#pragma unroll
-            for (int r = 0; r < GS; ++r) old[r] = __ldcg(s1 + S::T * (g0 + r));
-#pragma unroll
-            for (int r = 0; r < GS; ++r) s1[S::T * (g0 + r)] = old[r] + (double)acc1[g0 + r];
-        }
-#endif
         if (OBJ) {
             double2 *os = p.Osum + (size_t)ry * N + j;
 #pragma unroll
@@ -620,7 +593,6 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         // A thread owns pixel pairs (2 (j + T r), 2 (j + T r) + 1).  With the object sums
         // live, smaller groups keep the registers within the launch bound.
         constexpr int GS = OBJ ? 2 : 8;  // S1 pixel pairs per group
-#if SSB_S1_DF
         float4 *s1 = reinterpret_cast<float4 *>(p.S1 + (size_t)ry * N) + j;
 #pragma unroll
         for (int g0 = 0; g0 < 8; g0 += GS) {
@@ -634,19 +606,6 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
                 s1[S::T * (g0 + r)] = make_float4(a.x, a.y, c.x, c.y);
             }
         }
-#else
-        double2 *s1 = reinterpret_cast<double2 *>(p.S1 + (size_t)ry * N) + j;
-#pragma unroll
-        for (int g0 = 0; g0 < 8; g0 += GS) {
-            double2 old[GS];
-#pragma unroll
-            for (int r = 0; r < GS; ++r) old[r] = __ldcg(s1 + S::T * (g0 + r));
-#pragma unroll
-            for (int r = 0; r < GS; ++r)
-                s1[S::T * (g0 + r)] = make_double2(old[r].x + (double)acc1[2 * (g0 + r)],
-                                                   old[r].y + (double)acc1[2 * (g0 + r) + 1]);
-        }
-#endif
         if (OBJ) {
             double2 *os = p.Osum + (size_t)ry * N + 2 * j;  // pixel 2 (j + T r) + e at 2 T r + e
 #pragma unroll
@@ -732,9 +691,9 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
     }
     for (int i = tid; i < N; i += kFusedThreads) smem[S::OFF_TW + lay(i)] = p.tw[i];
     for (int i = tid; i < S::M; i += kFusedThreads) smem[S::OFF_TW2 + lay(i)] = p.tw[2 * i];
-    unsigned *err = p.sync;  // cleared once per library call, so a timeout stays raised
-    unsigned *ticket = p.sync + 1;
-    unsigned *col_done = p.sync + 2;
+    unsigned *err = p.err;
+    unsigned *ticket = p.sync;
+    unsigned *col_done = p.sync + 1;
     unsigned *plane_free = col_done + p.nbatch;
     unsigned *h_cnt = plane_free + (size_t)p.nbatch * p.Bk;
     unsigned *chain = h_cnt + (size_t)p.nbatch * p.Bk;
@@ -771,14 +730,10 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
             }
             __syncthreads();
             if (!SSB1 && s_nyq) {
-                // whole warps (the transforms synchronise the warp): warp 0 the Nyquist-row
-                // term, warp 1 the column N/2
-                if (tid < 32 && ok)
+                if (tid < 32 && ok)  // whole warp: the transform synchronises the warp
                     nyquist_transform<N>(p, smem + S::OFF_FFT + (tid / S::T) * S::SMF,
                                          smem + S::OFF_TW, smem + S::OFF_TW2, task.b % p.D, kk,
                                          tid % S::T, tid < S::T);
-                else if (tid >= 32 && tid < 64 && ok)
-                    half_column<N>(p, smem, task.b, kk);
                 __syncthreads();
                 if (tid == 0) {
                     fence_acq_rel();  // publishes Rp
@@ -861,10 +816,10 @@ static int row_tasks_for(int N) {
     return N / std::min(groups, N);
 }
 
-// error word, scheduler words, then the loss kernel's block counter (the last word)
+// scheduler words, then the loss kernel's block counter (the last word)
 size_t fused_sync_words(int N, int n_bf, int Bk) {
     const int nbatch = (n_bf + Bk - 1) / Bk;
-    return 2 + (size_t)nbatch * (1 + 2 * (size_t)Bk) + (size_t)row_tasks_for(N) + 1;
+    return 1 + (size_t)nbatch * (1 + 2 * (size_t)Bk) + (size_t)row_tasks_for(N) + 1;
 }
 
 static size_t ldz_for(int N) { return (size_t)((N / 2 + 1 + 7) / 8 * 8); }
@@ -950,10 +905,10 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     if ((e = cudaMemsetAsync(a.S2g, 0, sizeof(double) * S::NR, s)) != cudaSuccess) return e;
     if (want_object && (e = cudaMemsetAsync(a.Osum, 0, sizeof(double2) * P, s)) != cudaSuccess)
         return e;
-    // every scheduler word but the error word (word 0), which the caller clears once per
-    // library call so that a wait that ran out in any trial of a batch is still reported
-    if ((e = cudaMemsetAsync(a.sync + 1, 0, sizeof(unsigned) * (fused_sync_words(N, a.n_bf, a.Bk) - 1),
-                             s)) != cudaSuccess)
+    // the scheduler words (the error word is the caller's, cleared once per library call so
+    // that a wait that ran out in any trial of a batch is still reported)
+    if ((e = cudaMemsetAsync(a.sync, 0, sizeof(unsigned) * fused_sync_words(N, a.n_bf, a.Bk), s)) !=
+        cudaSuccess)
         return e;
     FusedParams fp;
     fp.G = a.G;
@@ -968,6 +923,7 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     fp.S2g = a.S2g;
     fp.Osum = a.Osum;
     fp.sync = a.sync;
+    fp.err = a.err;
     fp.n_bf = a.n_bf;
     fp.Bk = a.Bk;
     fp.nbatch = nbatch;
@@ -980,7 +936,7 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     prof_begin("k_loss", s);
     k_loss_fused<<<kLossBlocks, kLossThreads, 0, s>>>(
         a.S1, a.S2g, S::NR, (int)P, 1.0 / a.n_bf, a.S2g + S::NR,
-        a.sync + fused_sync_words(N, a.n_bf, a.Bk) - 1, a.sync, loss_slot);
+        a.sync + fused_sync_words(N, a.n_bf, a.Bk) - 1, a.err, loss_slot);
     prof_end(s);
     count_launch();
     return cudaGetLastError();

@@ -56,6 +56,7 @@ struct ObjectiveArgs {
     float2 *rring;          // Nyquist-row transforms ring
     double *S2g;            // per row task sums of phi^2
     unsigned *sync;         // scheduler counters
+    unsigned *err;          // error word (raised by a wait that ran out)
     int Bk;                 // BF planes per batch
     int D;                  // ring slots
     int mode;               // 0 SSB2, 1 SSB1
@@ -78,7 +79,7 @@ size_t fused_rring_elems(int N, int Bk, int D);
 int fused_row_tasks(int N);
 size_t fused_s2g_elems(int N);  // per row task S2 sums, then the loss kernel's block partials
 // One full objective evaluation on the persistent fused kernel (accumulators and
-// scheduler words cleared first), loss written to *loss_slot.  The error word (sync[0]) is
+// scheduler words cleared first), loss written to *loss_slot.  The error word (a.err) is
 // not cleared here: the caller clears it once per library call and reads it at the end, so
 // a wait that ran out in any evaluation of the call is reported (and every later loss of
 // the call is NaN).

@@ -82,7 +82,7 @@ static cudaError_t scratch_base(unsigned char **out) {
 }
 
 struct NoallocLayout {
-    size_t E, S1, Z, h, rp, S2g, kgeo, kalpha, kturn, yx, tw, loss, sync, total;
+    size_t E, S1, Z, h, rp, S2g, kgeo, kalpha, kturn, yx, tw, loss, err, sync, total;
 };
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -104,6 +104,7 @@ static NoallocLayout noalloc_layout(int N, int n_bf) {
     L.yx = o;     o = up256(o + (size_t)n_bf * 2 * sizeof(float));
     L.tw = o;     o = up256(o + (size_t)N * sizeof(float2));
     L.loss = o;   o = up256(o + sizeof(double));
+    L.err = o;    o = up256(o + sizeof(unsigned));
     L.sync = o;   o = up256(o + fused_sync_words(N, n_bf, bk) * sizeof(unsigned));
     L.total = o;
     return L;
@@ -187,6 +188,7 @@ extern "C" ssb_status ssb_loss_noalloc(const ssb_geometry *g, const void *g_cach
     a.rring = (float2 *)(base + L.rp);
     a.S2g = (double *)(base + L.S2g);
     a.sync = (unsigned *)(base + L.sync);
+    a.err = (unsigned *)(base + L.err);
     a.Bk = g->n_bf < kNoallocBk ? g->n_bf : kNoallocBk;
     a.D = kNoallocRing;
     a.mode = 0;
@@ -199,7 +201,7 @@ extern "C" ssb_status ssb_loss_noalloc(const ssb_geometry *g, const void *g_cach
     // accumulators and the other scheduler words are cleared by the objective itself)
     e = cudaMemcpyAsync(base + L.yx, g->bf_det_yx, sizeof(float) * 2 * (size_t)g->n_bf,
                         cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(a.sync, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.err, 0, sizeof(unsigned), s);
     if (e == cudaSuccess) {
         k_noalloc_geometry<<<(g->n_bf + 127) / 128, 128, 0, s>>>(
             (const float *)(base + L.yx), g->n_bf, a.dalpha, a.semi, (float4 *)(base + L.kgeo),
@@ -216,7 +218,7 @@ extern "C" ssb_status ssb_loss_noalloc(const ssb_geometry *g, const void *g_cach
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(&loss, a.loss, sizeof(double), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess)
-        e = cudaMemcpyAsync(&err_word, a.sync, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
+        e = cudaMemcpyAsync(&err_word, a.err, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
