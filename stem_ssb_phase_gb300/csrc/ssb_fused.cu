@@ -20,7 +20,8 @@
 //
 // Tasks (ticket order, phase p = [columns of batch p, rows of batch p-1]):
 //   column task (batch b, plane, CW columns, kColsPerWarp per warp): G load, correction,
-//       column IFFT, store to the ring slot, one column contiguous, Z[slot][plane][nx][ry];
+//       column IFFT, store to the ring slot, one column contiguous, Z[slot][plane][nx][ry]
+//       (SSB2 columns 0 < nx < N/2 as Z - (-1)^ry h(nx), the form the row rebuild uses);
 //       columns with exactly zero transfer store zeros without the work; for SSB2 the
 //       task that completes a plane's column pass also transforms its Nyquist-row term;
 //   row task (batch b, RT rows): for each plane of the batch, rebuild the full rows (SSB2)
@@ -93,7 +94,11 @@ struct FusedShape {
     static constexpr int M = SSB1 ? N : N / 2;      // row transform length
     static constexpr int RE = SSB1 ? kPts : 8;      // row transform points per thread (M / T)
     static constexpr int CW = GROUPS * kColsPerWarp;  // columns per column task
-    static constexpr int RT = GROUPS < N ? GROUPS : N;  // rows per row task (multiple of 4)
+    // rows per row task (multiple of 4), one per transform group.  (Two rows per warp --
+    // 16-row tasks with conflict-free 128-bit tile reads and interleaved row transforms --
+    // made the row work 27 % cheaper but released ring planes later, so that column tasks
+    // waited for free slots: slower overall.)
+    static constexpr int RT = GROUPS < N ? GROUPS : N;
     // Column tasks per plane.  (For SSB2 at N = 512 the last of the 17 takes column N/2
     // alone; moving that column into the task that completes the plane, beside the
     // Nyquist-row term, measured slower: it lengthens each plane's critical path.)
@@ -127,7 +132,7 @@ struct FusedShape {
     // [2][TILEBUF]; tensor-copy destinations start on a 1024-byte boundary (128 float2)
     static constexpr int OFF_TILE = TMA ? (OFF_RFFT + GROUPS * SMR + 127) / 128 * 128
                                         : OFF_RFFT + (GROUPS * SMR + 1) / 2 * 2;
-    static constexpr int TILEBUF = SSB1 ? H * LDC : H * LDC + LDZ + M;  // segments (, h, Rp)
+    static constexpr int TILEBUF = SSB1 ? H * LDC : H * LDC + M;  // segments (, Rp)
     static constexpr int U_COL = GROUPS * SMF;
     // cp.async tiles are triple-buffered (one block barrier per plane), tensor-copy tiles
     // double-buffered
@@ -268,13 +273,15 @@ __device__ void nyquist_transform(const FusedParams &p, float2 *fsm, const float
 // warp must call it (the transform synchronises the warp).
 // SSB1 column nx > N/2 reads the cache's column N - nx at the mirrored rows, conjugated
 // (G(-Q) = conj G(Q)).
+// column_correct does the loads and the correction (returning the warp-uniform skip
+// decision); column_compute adds the transform and, for SSB2, the h term (column_sub_h).
 template <int N, bool SSB1>
-__device__ __forceinline__ void column_compute(const FusedParams &p, float2 *smem, int k, int nx,
-                                               bool valid, const float4 &geo, const uint2 &bt,
+__device__ __forceinline__ bool column_correct(const FusedParams &p, int k, int nx, bool valid,
+                                               const float4 &geo, const uint2 &bt,
                                                float2 (&v)[kPts], float2 &hval, bool &hstore) {
     using S = FusedShape<N, SSB1>;
     constexpr int HG = N / 2 + 1;  // columns of the half-plane G cache
-    const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
+    const int j = threadIdx.x % S::T;
     const int sx = nx < N / 2 ? nx : nx - N;
     const bool zero = nx > 0 && (!(geo.z > 0.0f) || (SSB1 ? column_zero1(sx, geo.x, geo.y, p.tc)
                                                            : column_zero(sx, geo.x, geo.y, p.tc)));
@@ -331,8 +338,36 @@ __device__ __forceinline__ void column_compute(const FusedParams &p, float2 *sme
 #pragma unroll
         for (int r = 0; r < kPts; ++r) v[r] = make_float2(0.f, 0.f);
     }
-    if (!skip)
+    return skip;
+}
+
+// After the column transform (SSB2): store Z(ry, nx) - (-1)^ry h(nx), the form the row
+// rebuild needs (the C2R split of the row task): h(nx) is held by the group's first
+// thread; row ry = j + T r has the parity of j.  Columns 0 and N/2 carry no h.  Whole warp.
+template <int N>
+__device__ __forceinline__ void column_sub_h(int nx, bool valid, float2 (&v)[kPts], float2 hval) {
+    using S = FusedShape<N, false>;
+    const int tid = threadIdx.x, j = tid % S::T;
+    const int src = (tid & 31) - j;
+    const float hx = __shfl_sync(0xffffffffu, hval.x, src);
+    const float hy = __shfl_sync(0xffffffffu, hval.y, src);
+    if (valid && nx >= 1 && nx < N / 2) {
+        const float s = (j & 1) ? -1.0f : 1.0f;
+#pragma unroll
+        for (int r = 0; r < kPts; ++r) v[r] = make_float2(fmaf(-s, hx, v[r].x), fmaf(-s, hy, v[r].y));
+    }
+}
+
+template <int N, bool SSB1>
+__device__ __forceinline__ void column_compute(const FusedParams &p, float2 *smem, int k, int nx,
+                                               bool valid, const float4 &geo, const uint2 &bt,
+                                               float2 (&v)[kPts], float2 &hval, bool &hstore) {
+    using S = FusedShape<N, SSB1>;
+    const int grp = threadIdx.x / S::T, j = threadIdx.x % S::T;
+    if (!column_correct<N, SSB1>(p, k, nx, valid, geo, bt, v, hval, hstore)) {
         reg_fft<N, kPts, +1>(v, smem + S::OFF_FFT + grp * S::SMF, smem + S::OFF_TW, j, warp_bar);
+        if (!SSB1) column_sub_h<N>(nx, valid, v, hval);
+    }
 }
 
 // Store a transformed column into its ring plane (and h(nx), SSB2).
@@ -405,12 +440,9 @@ __device__ __forceinline__ void row_issue(const FusedParams &p, int slot, int kk
         cp_async_commit();
         return;
     }
-    const float2 *hsrc = p.hrow + ((size_t)slot * p.Bk + kk) * S::LDZ;
-    for (int e = threadIdx.x; e < S::LDZ / 2; e += kFusedThreads)
-        cp_async16(buf + S::H * S::LDC + 2 * e, hsrc + 2 * e);
     const float2 *rsrc = p.rrow + ((size_t)slot * p.Bk + kk) * S::M;
     for (int e = threadIdx.x; e < S::M / 2; e += kFusedThreads)
-        cp_async16(buf + S::H * S::LDC + S::LDZ + 2 * e, rsrc + 2 * e);
+        cp_async16(buf + S::H * S::LDC + 2 * e, rsrc + 2 * e);
     cp_async_commit();
 }
 
@@ -431,7 +463,8 @@ __device__ __forceinline__ void row_issue_tma(const FusedParams &p, const CUtens
 }
 
 // Row ry of the corrected image, split by symmetry (exact):
-//   Im c = real IFFT of Y(m) = -i (Z(m) - s h(m)) (0 < m < N/2), Y(0) = Im Z(0),
+//   Im c = real IFFT of Y(m) = -i (Z(m) - s h(m)) (0 < m < N/2; the ring already holds
+//          Z(m) - s h(m) for these columns, see column_compute), Y(0) = Im Z(0),
 //          Y(N/2) = Im Z(N/2), done as one N/2-point complex IFFT of
 //          V(m) = Y(m) + conj Y(N/2-m) + i (Y(m) - conj Y(N/2-m)) e^{2 pi i m/N},
 //          whose output holds Im c at pixels 2j (real part) and 2j+1 (imaginary part);
@@ -516,8 +549,7 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             }
         } else {
             const float2 *seg = cur + lr;               // element (nx, lr) at seg[nx * LDC]
-            const float2 *hs = cur + S::H * S::LDC;
-            const float2 *rp = hs + S::LDZ;
+            const float2 *rp = cur + S::H * S::LDC;
             const float2 z0 = seg[0], zm = seg[S::M * S::LDC];
             float2 v[8];
 #pragma unroll
@@ -527,11 +559,10 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
                 if (m == 0) {
                     ym = make_float2(z0.y, 0.f);
                     yc = make_float2(zm.y, 0.f);
-                } else {
-                    const float2 za = seg[m * S::LDC], ha = hs[m];
-                    const float2 zb = seg[mc * S::LDC], hb = hs[mc];
-                    ym = make_float2(fmaf(-sg, ha.y, za.y), fmaf(sg, ha.x, -za.x));
-                    yc = make_float2(fmaf(-sg, hb.y, zb.y), fmaf(sg, hb.x, -zb.x));
+                } else {  // the ring holds Z - s h for these columns
+                    const float2 za = seg[m * S::LDC], zb = seg[mc * S::LDC];
+                    ym = make_float2(za.y, -za.x);
+                    yc = make_float2(zb.y, -zb.x);
                 }
                 const float2 a = make_float2(ym.x + yc.x, ym.y - yc.y);
                 const float2 bb = cmul(make_float2(ym.x - yc.x, ym.y + yc.y), twid<+1>(twN, lay(m)));
@@ -896,13 +927,13 @@ static cudaError_t fused_launch(const FusedParams &fp, cudaStream_t s) {
 template <int N, bool SSB1>
 static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th, double *loss_slot,
                                      bool want_object, cudaStream_t s) {
-    using S = FusedShape<N, SSB1>;
+    constexpr int NR = FusedShape<N, SSB1>::NR;  // row tasks per trial
     cudaError_t e;
     if ((e = launch_theta_tables(a, th, s)) != cudaSuccess) return e;
     const size_t P = (size_t)N * N;
     const int nbatch = (a.n_bf + a.Bk - 1) / a.Bk;
     if ((e = cudaMemsetAsync(a.S1, 0, sizeof(double) * P, s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(a.S2g, 0, sizeof(double) * S::NR, s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.S2g, 0, sizeof(double) * NR, s)) != cudaSuccess) return e;
     if (want_object && (e = cudaMemsetAsync(a.Osum, 0, sizeof(double2) * P, s)) != cudaSuccess)
         return e;
     // the scheduler words (the error word is the caller's, cleared once per library call so
@@ -935,7 +966,7 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     if (e != cudaSuccess) return e;
     prof_begin("k_loss", s);
     k_loss_fused<<<kLossBlocks, kLossThreads, 0, s>>>(
-        a.S1, a.S2g, S::NR, (int)P, 1.0 / a.n_bf, a.S2g + S::NR,
+        a.S1, a.S2g, NR, (int)P, 1.0 / a.n_bf, a.S2g + NR,
         a.sync + fused_sync_words(N, a.n_bf, a.Bk) - 1, a.err, loss_slot);
     prof_end(s);
     count_launch();

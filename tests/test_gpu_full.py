@@ -41,15 +41,38 @@ def full_ref(full_case):
                                    workers=min(32, oracle.default_workers()))
 
 
-def test_full_size_loss_and_mean_phase_match_the_oracle(full_case, full_ref):
-    w, geom, host, ctx = full_case
-    theta, ref = full_ref  # the trial the benchmark times
-    mp, _, loss = ctx.reconstruct(theta, want_object=False)
-    assert abs(loss - ref["loss"]) <= 1e-5 * ref["loss"], (loss, ref["loss"])
+def _check_mean_phase(mp, ref):
     mask = ~ref["branch_cut"]
     err = np.abs(mp.cpu().numpy().astype(np.float64) - ref["mean_phase"])[mask]
     assert mask.mean() > 0.9
     assert err.max() <= 1e-4, (err.max(), int((err > 1e-4).sum()))
+
+
+def _check_object(gpu_obj, want, tol=1e-5, elem=1e-4):
+    """Relative L2 error and, element by element, the error against the largest modulus
+    (float32 rounding on these DC-dominated objects reaches 1.6e-5 of it)."""
+    o = gpu_obj.astype(np.complex128)
+    assert np.linalg.norm(o - want) <= tol * np.linalg.norm(want)
+    err = np.abs(o - want)
+    assert err.max() <= elem * np.abs(want).max(), err.max() / np.abs(want).max()
+
+
+def test_full_size_loss_and_mean_phase_match_the_oracle(full_case, full_ref):
+    w, geom, host, ctx = full_case
+    theta, ref = full_ref  # the trial the benchmark times
+    mp, obj, loss = ctx.reconstruct(theta, want_object=True)
+    assert abs(loss - ref["loss"]) <= 1e-5 * ref["loss"], (loss, ref["loss"])
+    _check_mean_phase(mp, ref)
+    _check_object(obj.cpu().numpy(), ref["object"])
+
+
+def test_full_size_at_the_generating_aberrations(full_case):
+    """A second full-size trial: the truth (small loss, phases concentrated near zero)."""
+    w, geom, host, ctx = full_case
+    mp, _, loss = ctx.reconstruct(w.truth, want_object=False)
+    ref = oracle.objective(geom, w.truth, counts=host, workers=min(32, oracle.default_workers()))
+    assert abs(loss - ref["loss"]) <= 1e-5 * ref["loss"], (loss, ref["loss"])
+    _check_mean_phase(mp, ref)
 
 
 def test_full_size_batch_equals_scalar_calls(full_case):
@@ -92,8 +115,7 @@ def test_full_size_upsampled_redraw_matches_the_oracle(full_case, full_ref):
     theta, ref = full_ref
     ph, obj, _ = ctx.reconstruct_upsampled(theta, 4)
     up = oracle.upsample_object(ref["object"], 4)
-    o = obj.cpu().numpy().astype(np.complex128)
-    assert np.linalg.norm(o - up) <= 1e-5 * np.linalg.norm(up)
+    _check_object(obj.cpu().numpy(), up)
     mask = np.abs(up) >= 0.05 * np.sqrt(np.mean(np.abs(up) ** 2))
     assert mask.mean() > 0.5
     d = np.angle(np.exp(1j * (ph.cpu().numpy().astype(np.float64) - np.angle(up))))[mask]
@@ -108,8 +130,7 @@ def test_full_size_redraw_without_loss_matches_the_oracle(full_case, full_ref):
     for f in (1, 4):
         ph, obj = ctx.redraw(theta, f)
         want = ref["object"] if f == 1 else oracle.upsample_object(ref["object"], f)
-        o = obj.cpu().numpy().astype(np.complex128)
-        assert np.linalg.norm(o - want) <= 1e-5 * np.linalg.norm(want)
+        _check_object(obj.cpu().numpy(), want)
         mask = np.abs(want) >= 0.05 * np.sqrt(np.mean(np.abs(want) ** 2))
         assert mask.mean() > 0.5
         d = np.angle(np.exp(1j * (ph.cpu().numpy().astype(np.float64) - np.angle(want))))[mask]

@@ -16,6 +16,8 @@ torch = pytest.importorskip("torch")
 
 LOSS_RTOL = 1e-5
 PHASE_ATOL = 1e-4
+OBJ_RTOL = 1e-5
+ELEM_RTOL = 1e-4  # element-wise error against the object's largest modulus
 
 
 @pytest.fixture(scope="module")
@@ -38,6 +40,17 @@ def small_data():
     w = ssb_synth.WORKLOADS["small"]
     geom, counts, phi = ssb_synth.simulate_counts_numpy(w)
     return w, geom, counts, phi
+
+
+def _check_object(gpu_obj, want, tol=OBJ_RTOL, elem=ELEM_RTOL):
+    """Object redraw: relative L2 error and, element by element, the error against the
+    object's largest modulus (a localised error in a few pixels fails the second; float32
+    rounding on these DC-dominated objects reaches 1.6e-5 of the largest modulus)."""
+    o = gpu_obj.astype(np.complex128)
+    scale = np.abs(want).max()
+    assert np.linalg.norm(o - want) <= tol * np.linalg.norm(want)
+    err = np.abs(o - want)
+    assert err.max() <= elem * scale, (err.max() / scale, np.unravel_index(int(err.argmax()), err.shape))
 
 
 def _check_phase(gpu_mp, ref, tol=PHASE_ATOL):
@@ -106,8 +119,7 @@ def test_tiny_objective(ssbgpu, tiny_data, transfer):
     mp, obj, loss = ctx.reconstruct(w.truth)
     ref = oracle.objective(geom, w.truth, counts=counts, mode=transfer, want_object=True)
     _check_phase(mp.cpu().numpy(), ref)
-    o = obj.cpu().numpy().astype(np.complex128)
-    assert np.linalg.norm(o - ref["object"]) <= 1e-5 * np.linalg.norm(ref["object"])
+    _check_object(obj.cpu().numpy(), ref["object"])
     assert abs(loss - ref["loss"]) <= LOSS_RTOL * ref["loss"]
 
 
@@ -136,8 +148,7 @@ def test_small_truth_phase_and_object(ssbgpu, small_data, transfer):
                            workers=_workers())
     assert abs(loss - ref["loss"]) <= LOSS_RTOL * ref["loss"]
     _check_phase(mp.cpu().numpy(), ref)
-    o = obj.cpu().numpy().astype(np.complex128)
-    assert np.linalg.norm(o - ref["object"]) <= 1e-5 * np.linalg.norm(ref["object"])
+    _check_object(obj.cpu().numpy(), ref["object"])
 
 
 @pytest.fixture(scope="module")
@@ -155,9 +166,10 @@ def test_medium_objective(ssbgpu, medium_data, transfer):
     thetas = np.vstack([np.array(w.truth)[None], ssb_synth.draw_trials(w, w.n_trials)])
     gpu = ctx.loss_batch(thetas)
     assert np.all(np.isfinite(gpu))
-    for j in (0, 1, 2):
+    # the truth, the first trials and trials spread over the batch (both buffer sets)
+    for j in (0, 1, 2, 67, 134, 200):
         ref = oracle.objective(geom, thetas[j], counts=counts, mode=transfer, workers=_workers())
-        assert abs(gpu[j] - ref["loss"]) <= LOSS_RTOL * ref["loss"]
+        assert abs(gpu[j] - ref["loss"]) <= LOSS_RTOL * ref["loss"], (j, gpu[j], ref["loss"])
     # object redraw at the best trial
     best = thetas[int(np.argmin(gpu))]
     mp, obj, loss = ctx.reconstruct(best)
@@ -165,6 +177,7 @@ def test_medium_objective(ssbgpu, medium_data, transfer):
     ref = oracle.objective(geom, best, counts=counts, mode=transfer, want_object=True,
                            workers=_workers())
     _check_phase(mp.cpu().numpy(), ref)
+    _check_object(obj.cpu().numpy(), ref["object"])
 
 
 # ---------------------------------------------------------------- edge cases

@@ -15,6 +15,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 OBJ_RTOL = 1e-5
+ELEM_RTOL = 1e-4  # element-wise error against the object's largest modulus
 PHASE_ATOL = 1e-4
 
 
@@ -55,6 +56,9 @@ def check_object(ph, obj, ref):
     o = obj.astype(np.complex128)
     rel = np.linalg.norm(o - ref) / np.linalg.norm(ref)
     assert rel <= OBJ_RTOL, rel
+    # element by element, against the largest modulus: a localised error fails here (float32
+    # rounding on these DC-dominated objects reaches 1.6e-5 of the largest modulus)
+    assert np.abs(o - ref).max() <= ELEM_RTOL * np.abs(ref).max()
     mask = np.abs(ref) >= 0.05 * np.sqrt(np.mean(np.abs(ref) ** 2))
     assert mask.mean() > 0.5
     d = np.abs(np.angle(np.exp(1j * (ph.astype(np.float64) - np.angle(ref)))))[mask]

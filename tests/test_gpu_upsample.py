@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 OBJ_RTOL = 1e-5
+ELEM_RTOL = 1e-4  # element-wise error against the object's largest modulus
 PHASE_ATOL = 1e-4
 
 
@@ -58,6 +59,9 @@ def check_upsampled(ph, obj, ref_obj, factor):
     o = obj.astype(np.complex128)
     rel = np.linalg.norm(o - up) / np.linalg.norm(up)
     assert rel <= OBJ_RTOL, rel
+    # element by element, against the largest modulus: a localised error fails here (float32
+    # rounding on these DC-dominated objects reaches 1.6e-5 of the largest modulus)
+    assert np.abs(o - up).max() <= ELEM_RTOL * np.abs(up).max()
     rms = np.sqrt(np.mean(np.abs(up) ** 2))
     mask = np.abs(up) >= 0.05 * rms
     assert mask.mean() > 0.5
