@@ -480,7 +480,7 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
     const int tid = threadIdx.x, grp = tid / S::T, j = tid % S::T;
     const int slot = b % p.D;
     const int ry0 = rt * S::RT;
-    const bool active = grp < S::RT;                // N = 32 leaves some groups idle
+    const bool active = S::RT >= S::GROUPS || grp < S::RT;  // N = 32 leaves some groups idle
     const int lr = active ? grp : 0;
     const int ry = ry0 + lr;
     const float sg = (ry & 1) ? -1.0f : 1.0f;       // (-1)^ry
@@ -595,13 +595,15 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
     if (SSB1 && active && *s_ok) {
         // pixel j + T r of row ry holds acc1[r]; loads are issued in groups ahead of their
         // stores (a store through the same pointer would hold back each following load)
+        // (the first batch writes its sums: the accumulators need no clearing)
         constexpr int GS = OBJ ? 4 : 16;
         float2 *s1 = reinterpret_cast<float2 *>(p.S1 + (size_t)ry * N) + j;
 #pragma unroll
         for (int g0 = 0; g0 < 16; g0 += GS) {
             float2 old[GS];
 #pragma unroll
-            for (int r = 0; r < GS; ++r) old[r] = __ldcg(s1 + S::T * (g0 + r));
+            for (int r = 0; r < GS; ++r)
+                old[r] = b == 0 ? make_float2(0.f, 0.f) : __ldcg(s1 + S::T * (g0 + r));
 #pragma unroll
             for (int r = 0; r < GS; ++r) s1[S::T * (g0 + r)] = df_add(old[r], acc1[g0 + r]);
         }
@@ -611,7 +613,8 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             for (int g0 = 0; g0 < 16; g0 += 4) {
                 double2 o[4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) o[r] = __ldcg(os + S::T * (g0 + r));
+                for (int r = 0; r < 4; ++r)
+                    o[r] = b == 0 ? make_double2(0.0, 0.0) : __ldcg(os + S::T * (g0 + r));
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
                     os[S::T * (g0 + r)] = make_double2(o[r].x + acco[g0 + r].x, o[r].y + acco[g0 + r].y);
@@ -623,13 +626,15 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         // pointer would otherwise hold back each following load for a full round trip.
         // A thread owns pixel pairs (2 (j + T r), 2 (j + T r) + 1).  With the object sums
         // live, smaller groups keep the registers within the launch bound.
+        // (the first batch writes its sums: the accumulators need no clearing)
         constexpr int GS = OBJ ? 2 : 8;  // S1 pixel pairs per group
         float4 *s1 = reinterpret_cast<float4 *>(p.S1 + (size_t)ry * N) + j;
 #pragma unroll
         for (int g0 = 0; g0 < 8; g0 += GS) {
             float4 old[GS];
 #pragma unroll
-            for (int r = 0; r < GS; ++r) old[r] = __ldcg(s1 + S::T * (g0 + r));
+            for (int r = 0; r < GS; ++r)
+                old[r] = b == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldcg(s1 + S::T * (g0 + r));
 #pragma unroll
             for (int r = 0; r < GS; ++r) {
                 const float2 a = df_add(make_float2(old[r].x, old[r].y), acc1[2 * (g0 + r)]);
@@ -641,7 +646,9 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
             double2 *os = p.Osum + (size_t)ry * N + 2 * j;  // pixel 2 (j + T r) + e at 2 T r + e
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
-                const double2 o0 = __ldcg(os + 2 * S::T * r), o1 = __ldcg(os + 2 * S::T * r + 1);
+                const double2 z = make_double2(0.0, 0.0);
+                const double2 o0 = b == 0 ? z : __ldcg(os + 2 * S::T * r);
+                const double2 o1 = b == 0 ? z : __ldcg(os + 2 * S::T * r + 1);
                 const float2 a0 = acco[2 * r], a1 = acco[2 * r + 1];
                 os[2 * S::T * r] = make_double2(o0.x + a0.x, o0.y + a0.y);
                 os[2 * S::T * r + 1] = make_double2(o1.x + a1.x, o1.y + a1.y);
@@ -659,7 +666,7 @@ __device__ void row_task(const FusedParams &p, float2 *smem, int b, int rt, int 
         double t = 0.0;
 #pragma unroll
         for (int w = 0; w < kFusedThreads / 32; ++w) t += red[w];
-        if (*s_ok) p.S2g[rt] = __ldcg(p.S2g + rt) + t;
+        if (*s_ok) p.S2g[rt] = (b == 0 ? 0.0 : __ldcg(p.S2g + rt)) + t;
     }
 }
 
@@ -732,8 +739,11 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
     // The ticket in s_ticket is read after the barrier at the top of the loop; thread 0
     // takes the next one only after the task's last barrier and its completion signals.
     if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
+    __syncthreads();
+    // Each task ends with a block barrier that publishes the next ticket in s_ticket (tid 0
+    // writes it again only after the next task's first barrier, which every warp reaches
+    // after reading it).
     while (true) {
-        __syncthreads();
         const Task task = decode_ticket<N, SSB1>(p, s_ticket);
         if (task.kind == 2) break;
         if (task.kind == 0) {
@@ -759,13 +769,17 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
                 if (!s_nyq) red_relaxed_add(col_done + task.b, 1u);
                 s_ticket = next;
             }
-            __syncthreads();
-            if (!SSB1 && s_nyq) {
-                if (tid < 32 && ok)  // whole warp: the transform synchronises the warp
+            __syncthreads();  // publishes s_ticket and s_nyq
+            if (!SSB1 && s_nyq && tid < 32) {
+                // Warp 0 alone transforms the plane's Nyquist terms and signals it, while the
+                // other warps go on to the next task.  Its scratch (the first N/2 + N/32 slots
+                // of the FFT region) is group 0's in either kind of task, so nothing the next
+                // task's other warps touch overlaps it.
+                if (ok)  // whole warp: the transform synchronises the warp
                     nyquist_transform<N>(p, smem + S::OFF_FFT + (tid / S::T) * S::SMF,
                                          smem + S::OFF_TW, smem + S::OFF_TW2, task.b % p.D, kk,
                                          tid % S::T, tid < S::T);
-                __syncthreads();
+                __syncwarp();
                 if (tid == 0) {
                     fence_acq_rel();  // publishes Rp
                     red_relaxed_add(col_done + task.b, 1u);
@@ -790,6 +804,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSM)
                 st_relaxed(chain + task.idx, (unsigned)task.b + 1u);
                 s_ticket = atomicAdd(ticket, 1u);
             }
+            __syncthreads();  // publishes s_ticket
         }
     }
 }
@@ -932,10 +947,8 @@ static cudaError_t fused_objective_n(const ObjectiveArgs &a, const TrialHost &th
     if ((e = launch_theta_tables(a, th, s)) != cudaSuccess) return e;
     const size_t P = (size_t)N * N;
     const int nbatch = (a.n_bf + a.Bk - 1) / a.Bk;
-    if ((e = cudaMemsetAsync(a.S1, 0, sizeof(double) * P, s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(a.S2g, 0, sizeof(double) * NR, s)) != cudaSuccess) return e;
-    if (want_object && (e = cudaMemsetAsync(a.Osum, 0, sizeof(double2) * P, s)) != cudaSuccess)
-        return e;
+    // (S1, the object sums and the per-row-task S2 are written, not added, by the first
+    // batch's row tasks, so they need no clearing here)
     // the scheduler words (the error word is the caller's, cleared once per library call so
     // that a wait that ran out in any trial of a batch is still reported)
     if ((e = cudaMemsetAsync(a.sync, 0, sizeof(unsigned) * fused_sync_words(N, a.n_bf, a.Bk), s)) !=

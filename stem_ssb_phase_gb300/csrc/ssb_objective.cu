@@ -24,10 +24,12 @@ __global__ void k_theta_E(float2 *__restrict__ Et, int N, double inv_nstep, doub
     const double qx = cr * fx - sr * fy, qy = sr * fx + cr * fy;
     // chi(lambda Q') / 2 pi = (lambda/2) Q'^T M Q'   (turns)
     const double t = 0.5 * lam * (m00 * qx * qx + 2.0 * m01 * qx * qy + m11 * qy * qy);
-    const double fr = t - rint(t);
-    double s, c;
-    sincospi(2.0 * fr, &s, &c);
-    Et[i] = make_float2((float)c, (float)s);
+    const double fr = t - rint(t);  // exact range reduction in float64, |fr| <= 1/2
+    // the table is complex64: the float32 function of the reduced angle is as accurate as
+    // rounding a float64 one, at a fraction of the float64 cost
+    float s, c;
+    sincospif((float)(2.0 * fr), &s, &c);
+    Et[i] = make_float2(c, s);
 }
 
 __device__ __forceinline__ uint32_t turn_fraction_u32(double turns) {
