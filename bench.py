@@ -381,6 +381,9 @@ def run_ours(args, rank, world, local_rank):
                                      "ssb_reconstruct at the result; host clock",
                          **fit}
 
+    if args.extras and rank == 0 and world == 1 and args.workload == "full" and not args.bf_subset:
+        extras["configs"] = config_table(cores)
+
     cpu = None
     if sample is not None:
         import oracle
@@ -458,6 +461,61 @@ def fit_workload(ctx, w, seed: int = 104) -> dict:
     return {"e2e_s": time.perf_counter() - t0, "search_s": t_search, "nelder_mead_s": t_nm,
             "nelder_mead_evaluations": len(evals), "best_trial": [float(x) for x in best],
             "fit_theta": [float(x) for x in theta], "fit_loss": float(loss)}
+
+
+def config_table(cores: int) -> dict:
+    """The smaller configurations: GPU ms per objective over each workload's own trial batch
+    (tiny: the truth; small: 16 trials; medium: 200 trials), and the float64 oracle on one
+    host core (tiny and small whole; medium on 256 evenly spaced BF pixels, scaled to all of
+    them by the BF count)."""
+    import torch
+
+    import stem_ssb_phase_gb300 as ssbgpu
+    out = {}
+    for name in ("tiny", "small", "medium"):
+        w = ssb_synth.WORKLOADS[name]
+        geom = ssb_synth.make_geometry(w)
+        if name == "medium":
+            _, counts_t, _ = ssb_synth.simulate_counts_torch(w, "cuda", geom=geom)
+            host = counts_t.cpu().numpy().view(np.uint32)
+            ctx = ssbgpu.SSB(geom, counts_t)
+            del counts_t
+        else:
+            _, host, _ = ssb_synth.simulate_counts_numpy(w, geom=geom)
+            ctx = ssbgpu.SSB(geom, host)
+        thetas = (np.array(w.truth)[None] if w.n_trials == 1
+                  else ssb_synth.draw_trials(w, w.n_trials))
+        for _ in range(3):
+            ctx.loss_batch(thetas)
+        reps = max(1, 200 // len(thetas))
+        stream = torch.cuda.current_stream()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            ctx.loss_batch(thetas)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ctx.close()
+        ms = e0.elapsed_time(e1) / (reps * len(thetas))
+        n = geom.scan_n
+        row = {"scan": n, "n_bf": geom.n_bf, "trials_per_batch": len(thetas),
+               "gpu_ms_per_objective": ms, "gpu_samples_per_s": geom.n_bf * n * n / (ms / 1e3)}
+        if name == "medium":
+            idx = np.linspace(0, geom.n_bf - 1, 256).astype(int)
+            sub = ssb_synth.make_geometry(w, bf_subset=idx)
+            t, _ = cpu_oracle_run(sub, host[idx], w.truth, workers=1)
+            t_all = t * geom.n_bf / len(idx)
+            row["oracle_single_core_s"] = t_all
+            row["oracle_sample"] = "256 of %d BF pixels on one core, scaled by the BF count" % geom.n_bf
+        else:
+            t_all, _ = cpu_oracle_run(geom, host, w.truth, workers=1)
+            row["oracle_single_core_s"] = t_all
+            row["oracle_sample"] = "all %d BF pixels on one core" % geom.n_bf
+        row["oracle_samples_per_s"] = geom.n_bf * n * n / t_all
+        out[name] = row
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_fit(args):
