@@ -5,7 +5,8 @@
 // so the per-BF inverse transforms, phases and moments of the objective are not needed:
 //   k_redraw_sum      sum over the BF pixels of the corrected spectra C_k (the same
 //                     correction as the objective), in fixed slices of the BF range;
-//                     float32 within runs of 32 BF, float64 across them
+//                     float32 within runs of 32 BF, float64 across them (a float pair by
+//                     exact two-sums instead measured slower here)
 //   k_redraw_combine  the slices added in slice order; for SSB2 the other half plane from
 //                     the anti-Hermitian symmetry of the corrected spectrum
 //   k_redraw_fft      one 2-D inverse transform of the N x N sum (register FFTs over
@@ -82,28 +83,39 @@ __device__ __forceinline__ void rd_load(const float2 *__restrict__ G, int k, int
 }
 
 // Block (x: column group, y: BF slice).  Thread jj of a column holds rows jj + TPC r.  The
-// slice's per-BF geometry is staged in shared memory, and the G values of the next plane
-// are loaded while the current plane is corrected.
+// slice's per-BF geometry is staged in shared memory in the form the column terms need --
+// u = alpha_k . (cos, sin) of the scan rotation, q u, q w and |alpha_k|^2 (q = lam_q), the
+// very float expressions of column_zero and col_geom, evaluated once per BF pixel instead of
+// once per column and BF pixel -- and the G values of the next plane are loaded while the
+// current plane is corrected.
 template <int N, bool SSB1>
 __global__ void __launch_bounds__(kRdThreads) k_redraw_sum(RedrawArgs p) {
     constexpr int TPC = N / kRdBins;                      // threads per column
     constexpr int CPB = TPC >= kRdThreads ? 1 : kRdThreads / TPC;  // columns per block
     constexpr int NCOL = SSB1 ? N : N / 2 + 1;
     static_assert(TPC <= kRdThreads && kRdThreads % TPC == 0, "column split");
-    extern __shared__ float4 rd_geo[];                    // [kps], then uint2 [kps]
+    extern __shared__ float4 rd_geo[];  // [kps] (u, q u, q w, |alpha|^2), uint2 [kps], float [kps] a_k
     uint2 *rd_bt = (uint2 *)(rd_geo + p.kps);
+    float *rd_a = (float *)(rd_bt + p.kps);
     const int k0 = blockIdx.y * p.kps, k1 = min(p.n_bf, k0 + p.kps);
     const int nk = max(0, k1 - k0);
+    const TrialConst &tc = p.tc;
     for (int i = threadIdx.x; i < nk; i += kRdThreads) {
-        rd_geo[i] = __ldg(p.kgeo + k0 + i);
+        const float4 g = __ldg(p.kgeo + k0 + i);
+        const float q = tc.lam_q;
+        const float u = fmaf(g.x, tc.cr, g.y * tc.sr), w = fmaf(g.y, tc.cr, -g.x * tc.sr);
+        rd_geo[i] = make_float4(u, q * u, q * w, fmaf(g.x, g.x, g.y * g.y));
         rd_bt[i] = __ldg(p.kturn + k0 + i);
+        rd_a[i] = g.z;
     }
     __syncthreads();
     const int jj = threadIdx.x % TPC;
     const int nx = blockIdx.x * CPB + threadIdx.x / TPC;
     if (nx >= NCOL) return;  // no block-level synchronisation below
     const int sx = nx < N / 2 ? nx : nx - N;
-    const TrialConst &tc = p.tc;
+    const float fsx = (float)sx;
+    const float osx = tc.lam_q * fsx;           // the column's offset along the rotated axis
+    const float q2 = tc.lam_q * tc.lam_q, sx2 = fsx * fsx;
     float2 e[kRdBins];
 #pragma unroll
     for (int r = 0; r < kRdBins; ++r) e[r] = __ldg(p.E + (size_t)nx * N + jj + TPC * r);
@@ -120,21 +132,28 @@ __global__ void __launch_bounds__(kRdThreads) k_redraw_sum(RedrawArgs p) {
     }
     double2 totm = make_double2(0.0, 0.0);
     float2 accm = make_float2(0.f, 0.f);
-    auto is_zero = [&](float4 geo) {
-        return nx > 0 && (!(geo.z > 0.0f) || (SSB1 ? column_zero1(sx, geo.x, geo.y, tc)
-                                                   : column_zero(sx, geo.x, geo.y, tc)));
+    // column_zero / column_zero1 of BF pixel i of the slice, from its staged u
+    auto is_zero = [&](int i) {
+        const float u = rd_geo[i].x;
+        return nx > 0 && (!(rd_a[i] > 0.0f) ||
+                          (fabsf(u - osx) >= tc.zero_r && (SSB1 || fabsf(u + osx) >= tc.zero_r)));
     };
     float2 gv[kRdBins], gn[kRdBins];
-    bool zero = nk > 0 ? is_zero(rd_geo[0]) : true;
+    bool zero = nk > 0 ? is_zero(0) : true;
     rd_load<N, SSB1>(p.G, k0, nx, jj, zero, gv);
     for (int it = 0; it < nk; ++it) {
         const float4 geo = rd_geo[it];
         const uint2 bt = rd_bt[it];
-        const bool zn = it + 1 < nk ? is_zero(rd_geo[it + 1]) : true;
+        const bool zn = it + 1 < nk ? is_zero(it + 1) : true;
         rd_load<N, SSB1>(p.G, k0 + it + 1, nx, jj, zn, gn);
         if (!zero) {
-            const bool active = geo.z > 0.0f;
-            const ColGeom cg = col_geom(sx, geo.x, geo.y, tc);
+            const bool active = rd_a[it] > 0.0f;
+            // col_geom's terms: base = q^2 sx^2 + |alpha|^2, p0 = (q u) sx, qw = q w
+            ColGeom cg;
+            cg.q2 = q2;
+            cg.base = fmaf(q2, sx2, geo.w);
+            cg.p0 = geo.y * fsx;
+            cg.qw = geo.z;
             const uint32_t phx = bt.x * (uint32_t)sx;
 #pragma unroll
             for (int r = 0; r < kRdBins; ++r) {
@@ -240,7 +259,7 @@ cudaError_t redraw_n(RedrawArgs &r, cudaStream_t s) {
     constexpr int TPC = N / kRdBins;
     constexpr int CPB = TPC >= kRdThreads ? 1 : kRdThreads / TPC;
     constexpr int NCOL = SSB1 ? N : N / 2 + 1;
-    const size_t smem = (sizeof(float4) + sizeof(uint2)) * (size_t)r.kps;
+    const size_t smem = (sizeof(float4) + sizeof(uint2) + sizeof(float)) * (size_t)r.kps;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k_redraw_sum<N, SSB1>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
