@@ -18,7 +18,9 @@
  *   c_k(r)     = IFFT2[C_k](r),  phi_k(r) = atan2(Im c_k, Re c_k)
  *   loss       = (1/P) sum_r [ S2(r)/n_bf - (S1(r)/n_bf)^2 ],  S1 = sum_k phi_k, S2 = sum_k phi_k^2
  *   chi(alpha) = (pi/lambda) [C10 |alpha|^2 + C12 ((ax^2 - ay^2) cos 2phi12 + 2 ax ay sin 2phi12)]
- *   a(alpha)   = clip((alpha_c - |alpha|)/d_alpha + 1/2, 0, 1)
+ *   a(alpha)   = clip((alpha_c - |alpha|)/d_alpha + 1/2, 0, 1), taken as 0 below 2^-16
+ *                (an aperture edge that a scan grid commensurate with the detector hits
+ *                exactly transmits nothing, whatever the rounding)
  * C10, C12 in nm; angles in rad; lambda and the scan step in Angstrom.
  *
  * Conventions for every entry point:
@@ -110,7 +112,8 @@ ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *lo
  * "object redraw"; page "SSB performance notes": phase-of-mean output).
  *   mean_phase_out: device [N][N] float32, S1/n_bf            (required)
  *   object_c64_out: device [N][N] complex64 interleaved, (1/n_bf) sum_k c_k   (nullable)
- *   loss_out:       host, one float64                          (nullable)           */
+ *   loss_out:       host, one float64                          (nullable)
+ * SSB_ERR_TIMEOUT as for ssb_loss_batch (the outputs are then unspecified). */
 ssb_status ssb_reconstruct(ssb_ctx *c, const ssb_params *theta, float *mean_phase_out,
                            float *object_c64_out, double *loss_out, void *cuda_stream);
 

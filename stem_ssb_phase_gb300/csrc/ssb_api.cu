@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <limits>
 #include <new>
 #include <string>
 #include <vector>
@@ -131,9 +132,12 @@ struct ssb_ctx {
     double2 *rd_part = nullptr;
     float2 *rd_S = nullptr, *rd_T = nullptr;
     // test hook (ssb_debug_stall_next): the evaluation with this index in the next call
-    // stalls its row tasks on a count that is never reached, with this poll limit
+    // stalls its row tasks on a count that is never reached, with this poll limit; the
+    // call_* copies are the hook as the current call took it over
     int dbg_stall_eval = -1;
     unsigned dbg_wait_limit = 0;
+    int call_stall_eval = -1;
+    unsigned call_wait_limit = 0;
 
     ObjectiveArgs args(int si = 0) const {
         const TrialSet &t = set[si];
@@ -192,25 +196,28 @@ static bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
 static cudaError_t evaluate(const ssb_ctx *c, const ssb_params &theta, double *loss_slot,
                             bool want_object, cudaStream_t s, int index = 0, int si = 0) {
     ObjectiveArgs a = c->args(si);
-    if (index == c->dbg_stall_eval) {
+    if (index == c->call_stall_eval) {
         a.stall = 1;
-        a.wait_limit = c->dbg_wait_limit;
+        a.wait_limit = c->call_wait_limit;
     }
     return run_objective_fused(a, theta, loss_slot, want_object, s);
 }
 
-// Start of a library call that evaluates the objective: clear the scheduler's error word
-// (it stays raised for the rest of the call once a wait has run out).
-static ssb_status begin_call(const ssb_ctx *c, cudaStream_t s) {
+// Start of a library call that evaluates the objective: take over (and so consume) the
+// stall test hook, whatever the call's outcome, and clear the scheduler's error word (it
+// stays raised for the rest of the call once a wait has run out).
+static ssb_status begin_call(ssb_ctx *c, cudaStream_t s) {
+    c->call_stall_eval = c->dbg_stall_eval;
+    c->call_wait_limit = c->dbg_wait_limit;
+    c->dbg_stall_eval = -1;
+    c->dbg_wait_limit = 0;
     SSB_CK(cudaMemsetAsync(c->err, 0, sizeof(unsigned), s));
     return SSB_OK;
 }
 
-// End of such a call: the scheduler's error word (a bounded wait that ran out in any of
-// the call's evaluations); consumes the stall test hook.
+// End of such a call, or of one chunk of it: the scheduler's error word (a bounded wait
+// that ran out in any of the call's evaluations so far).
 static ssb_status check_sync(ssb_ctx *c, cudaStream_t s) {
-    c->dbg_stall_eval = -1;
-    c->dbg_wait_limit = 0;
     unsigned h = 0;
     SSB_CK(cudaMemcpyAsync(&h, c->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
     SSB_CK(cudaStreamSynchronize(s));
@@ -462,8 +469,12 @@ ssb_status ssb_loss_batch(ssb_ctx *c, const ssb_params *theta, int T, double *lo
         }
         SSB_CK(cudaMemcpyAsync(loss_out + t0, c->loss, sizeof(double) * tn, cudaMemcpyDeviceToHost, s));
         // the error word is cleared once per call, so this sees a wait that ran out in any
-        // trial so far (those trials and all later ones have NaN losses)
-        if ((st = check_sync(c, s)) != SSB_OK) return st;
+        // trial so far (those trials and all later ones of the chunk have NaN losses); the
+        // chunks after it are not evaluated and their losses are NaN too
+        if ((st = check_sync(c, s)) != SSB_OK) {
+            for (int t = t0 + tn; t < T; ++t) loss_out[t] = std::numeric_limits<double>::quiet_NaN();
+            return st;
+        }
     }
     return SSB_OK;
 }

@@ -76,6 +76,17 @@ def test_a_wait_that_runs_out_in_any_trial_is_reported(ssbgpu, tiny_ctx, stalled
     assert np.array_equal(ctx.loss_batch(thetas), ref)
 
 
+def test_the_hook_is_consumed_by_the_next_call_even_if_it_does_not_reach_it(ssbgpu, tiny_ctx):
+    ctx, thetas, ref = tiny_ctx
+    ctx.debug_stall_next(len(thetas) - 1, 64)
+    # a two-trial call evaluates neither that trial index nor beyond: it succeeds
+    assert np.array_equal(ctx.loss_batch(thetas[:2]), ref[:2])
+    # and has consumed the hook, so a call that does reach that index is exact too
+    st, out = _raw_loss_batch(ssbgpu, ctx, thetas)
+    assert st == 0
+    assert np.array_equal(out, ref)
+
+
 def test_a_wait_that_runs_out_in_reconstruct_is_reported(ssbgpu, tiny_ctx):
     ctx, thetas, ref = tiny_ctx
     ctx.debug_stall_next(0, 64)
