@@ -76,6 +76,30 @@ def test_a_wait_that_runs_out_in_any_trial_is_reported(ssbgpu, tiny_ctx, stalled
     assert np.array_equal(ctx.loss_batch(thetas), ref)
 
 
+def test_a_timeout_in_one_chunk_of_a_long_batch(ssbgpu, tiny_ctx):
+    """ssb_loss_batch evaluates long batches in chunks of 4,096 trials and checks the error
+    word after each: a wait that runs out leaves NaN for the rest of its chunk (set by the
+    loss kernel) and for the chunks not evaluated after it (set by the host)."""
+    ctx, thetas, ref = tiny_ctx
+    chunk = 4096
+    T = chunk + 5
+    big = np.resize(thetas, (T, thetas.shape[1]))
+    want = np.resize(ref, T)
+    ctx.debug_stall_next(10, 64)  # in the first chunk
+    st, out = _raw_loss_batch(ssbgpu, ctx, big)
+    assert st == SSB_ERR_TIMEOUT
+    assert np.array_equal(out[:9], want[:9])
+    assert out[9] == want[9] or np.isnan(out[9])  # overlaps the stalled launch
+    assert np.isnan(out[10:]).all()
+    ctx.debug_stall_next(chunk + 2, 64)  # in the second chunk
+    st, out = _raw_loss_batch(ssbgpu, ctx, big)
+    assert st == SSB_ERR_TIMEOUT
+    assert np.array_equal(out[:chunk + 1], want[:chunk + 1])
+    assert out[chunk + 1] == want[chunk + 1] or np.isnan(out[chunk + 1])
+    assert np.isnan(out[chunk + 2:]).all()
+    assert np.array_equal(ctx.loss_batch(thetas), ref)
+
+
 def test_the_hook_is_consumed_by_the_next_call_even_if_it_does_not_reach_it(ssbgpu, tiny_ctx):
     ctx, thetas, ref = tiny_ctx
     ctx.debug_stall_next(len(thetas) - 1, 64)
