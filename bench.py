@@ -519,7 +519,7 @@ def config_table(cores: int) -> dict:
 
 
 def run_fit(args):
-    """Full fit workload (BASELINE's fit configuration) as its own JSON line."""
+    """The full fit workload (a 200-trial batch, Nelder-Mead, the redraw) as its own JSON line."""
     import torch
 
     import stem_ssb_phase_gb300 as ssbgpu

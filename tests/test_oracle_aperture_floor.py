@@ -75,7 +75,7 @@ def _shifted(g, k, sgn, rot):
     return g.alpha_x[k] + sgn * (g.lam * lqx), g.alpha_y[k] + sgn * (g.lam * lqy)
 
 
-def _survey(name, rot):
+def _edge_census(name, rot):
     """Per (k, sign): the oracle's amplitudes, the exact ones on the points near the edge,
     and the tallies the pins need."""
     w = ssb_synth.WORKLOADS[name]
@@ -124,7 +124,7 @@ def _survey(name, rot):
 
 @pytest.mark.parametrize("name,rot", [("tiny", 0.0), ("small", 0.0)])
 def test_floor_zeroes_exactly_the_edge_points_on_unrotated_grids(name, rot):
-    _, s = _survey(name, rot)
+    _, s = _edge_census(name, rot)
     print(name, rot, {k: v for k, v in s.items() if k != "both_zero"})
     assert s["exact_zero_nonzero"] == 0
     assert s["max_err_above_floor"] <= 1e-12
@@ -135,7 +135,7 @@ def test_floor_zeroes_exactly_the_edge_points_on_unrotated_grids(name, rot):
 
 @pytest.mark.parametrize("name,rot,max_floored", [("tiny", 0.2, 0), ("small", math.radians(5.0), 16)])
 def test_floor_keeps_every_amplitude_above_it_on_rotated_grids(name, rot, max_floored):
-    _, s = _survey(name, rot)
+    _, s = _edge_census(name, rot)
     print(name, rot, {k: v for k, v in s.items() if k != "both_zero"})
     assert s["exact_zero_nonzero"] == 0
     assert s["max_err_above_floor"] <= 1e-12
@@ -147,7 +147,7 @@ def test_floor_keeps_every_amplitude_above_it_on_rotated_grids(name, rot, max_fl
 
 def test_transfer_is_exactly_zero_where_both_shifted_apertures_are(tiny_data):
     w, geom, _, _ = tiny_data
-    g, s = _survey("tiny", 0.0)
+    g, s = _edge_census("tiny", 0.0)
     theta = w.truth  # rotation 0: the grid is commensurate with the detector
     hits = 0
     for k in range(g.n_bf):
