@@ -204,8 +204,7 @@ ssb_status ssb_profile_end(ssb_kernel_time *out, int cap, int *n_out);
  * holds until the process exits; problems that do not fit (n_bf > 16384, or a layout
  * beyond 24 MiB) fail with SSB_ERR_ARG before any device work.  Set-up: the first call on
  * a device (and the first after that device's context was reset) looks up the array's
- * device address; make that first call before any stream capture.  *loss_out is written
- * only when the call returns SSB_OK.
+ * device address.  *loss_out is written only when the call returns SSB_OK.
  * Calls share the array and its contents persist between calls (what must start at zero
  * is cleared by each call), so calls that overlap on the GPU -- concurrent streams,
  * threads or devices sharing a call in flight -- race and must be serialised by the

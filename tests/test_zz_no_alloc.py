@@ -1,6 +1,6 @@
 """ssb_loss_noalloc, the entry point for callers that cannot allocate device memory
-(code under CUDA-graph stream capture, allocation-free real-time pipelines, plug-ins whose
-host application owns the GPU memory): through the C ABI, its loss must match
+(allocation-free real-time pipelines, plug-ins whose host application owns the GPU
+memory): through the C ABI, its loss must match
 ssb_loss_batch's on the same G cache within the tests' loss tolerance, on two calls in a
 row, and oversized problems must be refused before any device work.
 
