@@ -20,6 +20,15 @@
 #ifndef SSB_FUSED_RING
 #define SSB_FUSED_RING 4
 #endif
+// SSB1 (all N columns, twice the ring per plane): 10-plane batches in 3 slots, 60 MB at
+// N = 512 (8 planes in 4 slots measured 0.5 % slower, 6 in 4 slots 4 % slower, 16 in 2
+// slots 60 % slower)
+#ifndef SSB_FUSED_BK1
+#define SSB_FUSED_BK1 10
+#endif
+#ifndef SSB_FUSED_RING1
+#define SSB_FUSED_RING1 3
+#endif
 
 namespace ssb {
 
@@ -324,12 +333,12 @@ ssb_status ssb_prepare(const ssb_geometry *g, const void *counts, ssb_dtype dtyp
     // Both transfers run on the persistent fused kernel.  Batch size and ring depth: four
     // batches in flight keep the column work flowing while row tasks drain the oldest
     // slot, and the ring stays within L2 (67 MB at N = 512; SSB1 transforms all N columns,
-    // so its batches hold half the planes).  Larger batches amortise each row task's fixed
+    // so its ring holds 30 planes in 3 slots, 60 MB).  Larger batches amortise each row task's fixed
     // costs further but push the ring out of L2: at 24 planes and more the whole
     // intermediate round-trips HBM (about 3x the G bytes of DRAM traffic).
     const bool ssb1 = transfer == SSB_TRANSFER_SSB1;
-    c->Bk = std::min(ssb1 ? SSB_FUSED_BK / 2 : SSB_FUSED_BK, c->n_bf);
-    c->D = SSB_FUSED_RING;
+    c->Bk = std::min(ssb1 ? SSB_FUSED_BK1 : SSB_FUSED_BK, c->n_bf);
+    c->D = ssb1 ? SSB_FUSED_RING1 : SSB_FUSED_RING;
     for (TrialSet &t : c->set) {
         SSB_ALLOC(t.kturn, (size_t)c->n_bf, sb);
         SSB_ALLOC(t.E, P, sb);
