@@ -305,7 +305,7 @@ __device__ __forceinline__ bool column_correct(const FusedParams &p, int k, int 
             for (int r = 0; r < kPts; ++r) v[r] = cconj(__ldcs(g + ((N - j - S::T * r) & (N - 1))));
         }
 #pragma unroll
-        for (int r = 0; r < kPts; ++r) ev[r] = __ldg(e + S::T * r);
+        for (int r = 0; r < kPts; ++r) ev[r] = __ldcg(e + S::T * r);  // L2 only: 0.2 % faster than via L1
         const ColGeom cg = col_geom(sx, geo.x, geo.y, p.tc);
         const float fj = (float)j;
         const uint32_t phx = bt.x * (uint32_t)sx;
@@ -327,7 +327,7 @@ __device__ __forceinline__ bool column_correct(const FusedParams &p, int k, int 
                 // Nyquist row (ny = N/2): the mirror bin N - nx has no partner and
                 // carries its own correction, at signed bins (-nx, -N/2), where the
                 // column geometry has p0 negated
-                const float2 em = __ldg(p.Et + (size_t)(N - nx) * N + N / 2);
+                const float2 em = __ldcg(p.Et + (size_t)(N - nx) * N + N / 2);
                 ColGeom cm = cg;
                 cm.p0 = -cg.p0;
                 const float2 c2 = active ? correct_ssb2(cconj(gv), -(float)(N / 2), -N / 2, em, cm,
