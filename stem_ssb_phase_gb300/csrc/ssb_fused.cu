@@ -95,9 +95,10 @@ struct FusedShape {
     static constexpr int RE = SSB1 ? kPts : 8;      // row transform points per thread (M / T)
     static constexpr int CW = GROUPS * kColsPerWarp;  // columns per column task
     // rows per row task (multiple of 4), one per transform group.  (Two rows per warp --
-    // 16-row tasks with conflict-free 128-bit tile reads and interleaved row transforms --
-    // made the row work 27 % cheaper but released ring planes later, so that column tasks
-    // waited for free slots: slower overall.)
+    // 16-row tasks with 128-bit tile reads and interleaved row transforms -- measured slower
+    // in every form tried: whole-batch tasks release ring planes too late for the column
+    // tasks, half-batch tasks pay a second ordered update per batch, and the shared reads
+    // save only about 5 % of a row's instructions.)
     static constexpr int RT = GROUPS < N ? GROUPS : N;
     // Column tasks per plane.  (For SSB2 at N = 512 the last of the 17 takes column N/2
     // alone; moving that column into the task that completes the plane, beside the
