@@ -28,10 +28,9 @@
 //       or take them as they are (SSB1), row IFFT, phi = atan2, accumulate; then add the
 //       batch's per-pixel sums into S1 (a float pair per pixel, exact two-sum; S2 and the
 //       object in float64) in batch order.
-// A block takes its next ticket when its current task has finished its work: a column
-// task just before its completion fence (the round trips overlap), a row task after its
-// signal.  (Taking a column ticket any earlier, even just before the task's ring writes,
-// measured about 14 % slower overall.)  A task waits only for tasks holding smaller
+// A block takes its next ticket when its current task has finished its work, just before
+// the task's completion fence (the two round trips overlap).  (Taking a column ticket any
+// earlier, even just before the task's ring writes, measured about 14 % slower overall.)  A task waits only for tasks holding smaller
 // tickets, so the schedule cannot deadlock whatever the number of resident blocks.
 // Every wait is bounded; on timeout the kernel raises an error flag, all waits stop and
 // the host reports SSB_ERR_TIMEOUT.
